@@ -1,0 +1,127 @@
+"""float64 CPU oracle for the selective scan (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product (the CUDA library and its
+binding) never does: it shares no code with this module.
+
+The arithmetic lives in ``oracle.c`` (plain sequential loops in double
+precision); this module only compiles it with gcc and marshals numpy arrays.
+Every array is widened to float64 before the call, so the oracle sees exactly
+the values (bf16- or fp32-rounded) that the GPU path reads.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+DISC_SIMPLE = 0
+DISC_ZOH = 1
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so beside it (gcc, -O2, OpenMP)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB_PATH)
+        dp = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        ci = ctypes.c_int
+        lib.oracle_softplus.restype = ctypes.c_double
+        lib.oracle_softplus.argtypes = [ctypes.c_double]
+        lib.oracle_selective_scan.restype = None
+        lib.oracle_selective_scan.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, dp, dp, dp,
+                                              i64, i64, i64, i64]
+        lib.oracle_state_update.restype = None
+        lib.oracle_state_update.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, ci, ci, dp, i64, i64, i64]
+        lib.oracle_num_threads.restype = ci
+        lib.oracle_set_num_threads.argtypes = [ci]
+        _lib = lib
+    return _lib
+
+
+def _f64(a):
+    if a is None:
+        return None
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data
+
+
+def softplus(x: float) -> float:
+    return _load().oracle_softplus(float(x))
+
+
+def num_threads() -> int:
+    return _load().oracle_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    _load().oracle_set_num_threads(int(n))
+
+
+def selective_scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus_flag=True,
+                   h0=None, disc=DISC_SIMPLE, reverse=False):
+    """y[b,d,t], last_state[b,d,n] of the selective scan, in float64.
+
+    Shapes: u, delta, z: [Bsz, Dch, L]; B, C: [Bsz, N, L]; A: [Dch, N];
+    D, delta_bias: [Dch]; h0: [Bsz, Dch, N].
+    """
+    u, delta, A, B, C = (_f64(x) for x in (u, delta, A, B, C))
+    D, z, delta_bias, h0 = (_f64(x) for x in (D, z, delta_bias, h0))
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    if N > 4096:
+        raise ValueError("oracle supports N <= 4096")
+    assert delta.shape == u.shape and B.shape == (Bsz, N, L) and C.shape == (Bsz, N, L)
+    assert A.shape == (Dch, N)
+    assert z is None or z.shape == u.shape
+    assert D is None or D.shape == (Dch,)
+    assert delta_bias is None or delta_bias.shape == (Dch,)
+    assert h0 is None or h0.shape == (Bsz, Dch, N)
+    y = np.empty((Bsz, Dch, L), dtype=np.float64)
+    last = np.empty((Bsz, Dch, N), dtype=np.float64)
+    _load().oracle_selective_scan(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                  _ptr(delta_bias), int(bool(softplus_flag)), int(disc), int(bool(reverse)),
+                                  _ptr(h0), _ptr(y), _ptr(last), Bsz, Dch, L, N)
+    return y, last
+
+
+def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus_flag=True,
+                 disc=DISC_SIMPLE):
+    """One recurrent step.  Returns (y[b,d], new_state[b,d,n]); the input is not modified.
+
+    Shapes: state: [Bsz, Dch, N]; u, delta, z: [Bsz, Dch]; B, C: [Bsz, N];
+    A: [Dch, N]; D, delta_bias: [Dch].
+    """
+    st = _f64(state).copy()
+    u, delta, A, B, C = (_f64(x) for x in (u, delta, A, B, C))
+    D, z, delta_bias = (_f64(x) for x in (D, z, delta_bias))
+    Bsz, Dch, N = st.shape
+    if N > 4096:
+        raise ValueError("oracle supports N <= 4096")
+    assert u.shape == (Bsz, Dch) and delta.shape == (Bsz, Dch)
+    assert B.shape == (Bsz, N) and C.shape == (Bsz, N) and A.shape == (Dch, N)
+    y = np.empty((Bsz, Dch), dtype=np.float64)
+    _load().oracle_state_update(_ptr(st), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                _ptr(z), _ptr(delta_bias), int(bool(softplus_flag)), int(disc), _ptr(y),
+                                Bsz, Dch, N)
+    return y, st
