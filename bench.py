@@ -1,0 +1,504 @@
+"""Benchmark of the B300 selective scan: one JSON line on stdout.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one selective_scan_fwd over one batch of synthetic, seeded inputs of
+the workload (default: one Mamba-130M-shaped layer, batch 8, d_inner 1536,
+d_state 16, L 2048, bf16 I/O, fp32 state).  Inputs are resident in HBM; the
+step rotates over enough copies of them that the data one step reads exceeds
+the 126 MB L2, so no step finds the previous step's bytes in cache.
+
+Reported:
+  value       algorithmic HBM GB/s over all ranks (metric of the workload)
+  roofline    the scan kernel against the slower of HBM bytes at the measured
+              copy bandwidth and B*D*L*N exps at the MUFU ex2 peak
+  e2e         the same metric through the C-ABI call with pinned host buffers,
+              host->device inputs and device->host outputs inside the timed region
+  cpu_baseline the float64 oracle on the host cores (a bounded sample)
+Under torchrun every rank runs its own replica (weak scaling); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_148_b300 import inputs  # noqa: E402
+
+METRIC = "selective_scan_fwd achieved HBM GB/s (% of peak) and (B·L) tokens/s per layer"
+DEFAULT_WORKLOAD = "mamba130m_b8_d1536_n16_l2048_bf16"
+L2_BYTES = 126 * 1024 * 1024
+SM_COUNT_NOMINAL = 148
+SM_MAX_MHZ_NOMINAL = 2032.0
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), source="measured", sm_max_mhz=float(d.get("sm_max_mhz", 2032.0)))
+    return dict(hbm_gbs=6400.0, source="fallback", sm_max_mhz=SM_MAX_MHZ_NOMINAL)
+
+
+def io_bytes(io):
+    return 2 if io == "bf16" else 4
+
+
+def scan_bytes(Bsz, Dch, L, N, io, with_z=True):
+    """Algorithmic bytes of one scan: u, delta, (z) in, y out, B and C, A, D, bias, last_state."""
+    s = io_bytes(io)
+    return ((3 if with_z else 2) + 1) * Bsz * Dch * L * s + 2 * Bsz * N * L * s + Dch * N * 4 + 2 * Dch * 4 \
+        + Bsz * Dch * N * 4
+
+
+def step_bytes(Bsz, Dch, N, io):
+    """Algorithmic bytes of one decode step: state in and out, u/delta/z in, y out, B, C, A, D, bias."""
+    s = io_bytes(io)
+    return 2 * Bsz * Dch * N * 4 + 4 * Bsz * Dch * s + 2 * Bsz * N * s + Dch * N * 4 + 2 * Dch * 4
+
+
+# ----------------------------------------------------------------------------- clocks during the timed region
+
+class ClockSampler:
+    """Polls NVML (SM clock, throttle reasons) in a thread while the timed region runs."""
+
+    REASONS = {
+        0x0000000000000008: "hw_slowdown", 0x0000000000000020: "sw_thermal_slowdown",
+        0x0000000000000040: "hw_thermal_slowdown", 0x0000000000000004: "sw_power_cap",
+        0x0000000000000080: "hw_power_brake_slowdown", 0x0000000000000001: "gpu_idle",
+        0x0000000000000002: "applications_clocks_setting",
+    }
+
+    def __init__(self, device_index):
+        self.samples, self.reasons, self.max_mhz = [], set(), None
+        self._stop = threading.Event()
+        self._t = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self.nvml = pynvml
+            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
+        except Exception:
+            self.nvml = None
+
+    def _run(self):
+        p = self.nvml
+        while not self._stop.is_set():
+            try:
+                self.samples.append(p.nvmlDeviceGetClockInfo(self.h, p.NVML_CLOCK_SM))
+                r = p.nvmlDeviceGetCurrentClocksEventReasons(self.h)
+                for bit, name in self.REASONS.items():
+                    if r & bit and name != "gpu_idle":
+                        self.reasons.add(name)
+            except Exception:
+                break
+            time.sleep(0.002)
+
+    def __enter__(self):
+        if self.nvml is not None:
+            self._t = threading.Thread(target=self._run, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self._t is not None:
+            self._t.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ----------------------------------------------------------------------------- MUFU peak
+
+def mufu_ex2_per_clk_per_sm(m, torch):
+    """ex2 per SM per clock from the MUFU microbenchmark (all SMs, 2048 threads each)."""
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    sms = props.multi_processor_count
+    blocks, threads, iters = sms * 8, 256, 4096
+    cycles = torch.zeros(blocks, dtype=torch.int64, device="cuda")
+    sink = torch.empty(blocks * threads, dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        m.mamba_bench_ex2(cycles, sink, iters, blocks, threads)
+    torch.cuda.synchronize()
+    cyc = int(cycles.max().item())
+    total = blocks * threads * iters * 8
+    return total / (sms * cyc), sms
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) timing
+
+def time_oracle(x, budget_s=12.0):
+    """Oracle over whole time rows of a growing subset of channels; returns (bytes/s, updates/s, info)."""
+    import oracle
+    Bsz, Dch, L, N = x.shape
+    threads = oracle.num_threads()
+    chans_total = Bsz * Dch
+
+    def run(nch):
+        b_idx = [c // Dch for c in range(nch)]
+        d_idx = [c % Dch for c in range(nch)]
+        # group by batch so each oracle call sees one batch's B and C
+        t_cpu = 0.0
+        for b in sorted(set(b_idx)):
+            ds = [d for bb, d in zip(b_idx, d_idx) if bb == b]
+            lo, hi = min(ds), max(ds) + 1
+            sl = lambda a: inputs.to_f64(a[b:b + 1, lo:hi], x.io)
+            args = (sl(x.u), sl(x.delta), x.A[lo:hi].astype(np.float64), inputs.to_f64(x.B[b:b + 1], x.io),
+                    inputs.to_f64(x.C[b:b + 1], x.io), x.D[lo:hi].astype(np.float64), sl(x.z),
+                    x.delta_bias[lo:hi].astype(np.float64))
+            t0 = time.perf_counter()
+            oracle.selective_scan(*args)
+            t_cpu += time.perf_counter() - t0
+        return t_cpu
+
+    nch = min(chans_total, max(1, threads))
+    t = run(nch)
+    while t < budget_s / 4 and nch < chans_total:
+        nch = min(chans_total, int(nch * max(2.0, min(8.0, budget_s / 4 / max(t, 1e-3)))))
+        t = run(nch)
+    frac = nch / chans_total
+    bytes_s = scan_bytes(Bsz, Dch, L, N, x.io) * frac / t
+    return bytes_s, nch * N * L / t, dict(channels=nch, of=chans_total, seconds=t, threads=threads)
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(inputs.WORKLOADS) + [inputs.DECODE_WORKLOAD["name"]])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return reference_arm(args, world, rank)
+
+    import torch
+    import selective_state_space_148_b300 as m
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    m.lib()
+
+    decode = args.workload == inputs.DECODE_WORKLOAD["name"]
+    if decode:
+        res = bench_decode(args, m, torch)
+    else:
+        res = bench_scan(args, m, torch)
+
+    # max over ranks of the timed region
+    t_ms = res["ms_per_step"]
+    if dist is not None:
+        tt = torch.tensor([t_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_ms = float(tt.item())
+        te = torch.tensor([res["e2e_ms"]], device="cuda")
+        dist.all_reduce(te, op=dist.ReduceOp.MAX)
+        res["e2e_ms"] = float(te.item())
+    bytes_step = res["bytes"]
+    value = world * bytes_step / (t_ms * 1e-3) / 1e9
+    e2e_value = world * bytes_step / (res["e2e_ms"] * 1e-3) / 1e9
+    peaks = measured_peaks()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not decode:
+        bps, ups, info = time_oracle(res["inputs"])
+        cpu = {"value": bps / 1e9, "unit": "GB/s", "cores": info["threads"], "kind": "oracle",
+               "sample": f"float64 oracle over whole time rows of {info['channels']} of {info['of']} channels "
+                         f"of {args.workload} ({info['seconds']:.1f} s); value scaled to the workload's bytes",
+               "updates_per_s": ups}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC if not decode else "selective_state_update achieved HBM GB/s and tokens/s",
+            "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(t_ms, 6), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": res["dtype"], "data": "synthetic",
+            "config": res["config"],
+            "pct_of_hbm_peak": round(100.0 * value / world / peaks["hbm_gbs"], 2),
+            "tokens_per_s": round(world * res["tokens"] / (t_ms * 1e-3), 1),
+            "roofline": res["roofline"],
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": res["h2d"],
+                    "d2h_bytes_per_step": res["d2h"], "ms_per_step": round(res["e2e_ms"], 4),
+                    "tokens_per_s": round(world * res["tokens"] / (res["e2e_ms"] * 1e-3), 1)},
+            "gpu_launches": res["launches"],
+            "clocks": res["clocks"],
+            "mufu": res.get("mufu"),
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def traffic_record(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    rec = json.load(open(p)).get(kernel_key)
+    if not rec:
+        return None
+    if rec.get("source_sha") != kernel_source_sha():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_148_b300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def bench_scan(args, m, torch):
+    x = inputs.make_workload(args.workload)
+    Bsz, Dch, L, N = x.shape
+    io = x.io
+    tdt = torch.bfloat16 if io == "bf16" else torch.float32
+    dev = torch.device("cuda")
+
+    def d(a):
+        if io == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    base = dict(u=d(x.u), delta=d(x.delta), z=d(x.z), B=d(x.B), C=d(x.C))
+    A = torch.from_numpy(x.A).to(dev)
+    D = torch.from_numpy(x.D).to(dev)
+    bias = torch.from_numpy(x.delta_bias).to(dev)
+    nbytes = scan_bytes(Bsz, Dch, L, N, io)
+    R = max(2, math.ceil(3 * L2_BYTES / nbytes))           # rotation copies: > 3x L2 between reuses
+    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(R - 1)]
+    ys = [torch.empty_like(base["u"]) for _ in range(R)]
+    hs = [torch.empty((Bsz, Dch, N), dtype=torch.float32, device=dev) for _ in range(R)]
+    ws_bytes = m.mamba_scan_workspace_size(Bsz, Dch, L, N, 0, m.MAMBA_BF16 if io == "bf16" else m.MAMBA_F32)
+    chunked = ws_bytes > 0
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        s = sets[i % R]
+        m.mamba_selective_scan_fwd(s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, ys[i % R], hs[i % R],
+                                   stream=stream)
+
+    mufu_per_clk, sms = mufu_ex2_per_clk_per_sm(m, torch)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as cs:
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    t_ms = ev0.elapsed_time(ev1) / args.steps
+    clocks = cs.summary()
+
+    # end to end through the C ABI from pinned host buffers
+    hsrc = {k: v.cpu().pin_memory() for k, v in base.items()}
+    hy = torch.empty(base["u"].shape, dtype=tdt).pin_memory()
+    hh = torch.empty((Bsz, Dch, N), dtype=torch.float32).pin_memory()
+    dsets = sets[0]
+
+    def e2e_step(i):
+        for k in dsets:
+            dsets[k].copy_(hsrc[k], non_blocking=True)
+        m.mamba_selective_scan_fwd(dsets["u"], dsets["delta"], A, dsets["B"], dsets["C"], D, dsets["z"], bias, 1,
+                                   ys[0], hs[0], stream=stream)
+        hy.copy_(ys[0], non_blocking=True)
+        hh.copy_(hs[0], non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    h2d = sum(v.numel() * v.element_size() for v in hsrc.values())
+    d2h = hy.numel() * hy.element_size() + hh.numel() * hh.element_size()
+
+    peaks = measured_peaks()
+    exps = Bsz * Dch * L * N
+    t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
+    mufu_units = round(mufu_per_clk)
+    mufu_peak = SM_COUNT_NOMINAL * mufu_units * peaks["sm_max_mhz"] * 1e6   # ex2 per second
+    t_mufu = exps / mufu_peak
+    t_meas = t_ms * 1e-3
+    kernel = "scan_kernel<bf16,NP16,full>" if io == "bf16" and N <= 16 else f"scan_kernel<{io},N{N},full>"
+    traffic = traffic_record(f"{args.workload}")
+    if t_mufu >= t_hbm:
+        roof = {"bound": "alu", "achieved": round(exps / t_meas / 1e12, 4),
+                "peak": round(mufu_peak / 1e12, 4), "unit": "Tex2/s", "frac": round(t_mufu / t_meas, 4),
+                "traffic": traffic, "kernel": kernel,
+                "peak_source": f"{SM_COUNT_NOMINAL} SMs x {mufu_units} ex2/clk/SM (microbenchmark: "
+                               f"{mufu_per_clk:.2f}) x {peaks['sm_max_mhz']:.0f} MHz",
+                "hbm": {"achieved": round(nbytes / t_meas / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(t_hbm / t_meas, 4), "peak_source": peaks["source"]}}
+    else:
+        roof = {"bound": "hbm", "achieved": round(nbytes / t_meas / 1e9, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(t_hbm / t_meas, 4), "traffic": traffic, "kernel": kernel,
+                "peak_source": f"{peaks['source']} copy bandwidth"}
+    if chunked:
+        roof["note"] = "chunked scan: the step is three launches (chunk states, carry, rescan); figures are per step"
+    return dict(ms_per_step=t_ms, bytes=nbytes, tokens=Bsz * L, dtype="f32" if io == "f32" else "bf16",
+                config={"workload": args.workload, "batch": Bsz, "d_inner": Dch, "d_state": N, "seq_len": L,
+                        "io": io, "state": "fp32", "l2": f"inputs rotate over {R} resident copies "
+                                                          f"({R * nbytes / 1e6:.0f} MB > L2)",
+                        "path": "chunked" if chunked else "direct"},
+                roofline=roof, h2d=h2d, d2h=d2h, e2e_ms=e2e_ms, launches=args.steps * (3 if chunked else 1),
+                clocks=clocks, inputs=x,
+                mufu={"ex2_per_clk_per_sm": round(mufu_per_clk, 3), "sms": sms})
+
+
+def bench_decode(args, m, torch):
+    cfg = inputs.DECODE_WORKLOAD
+    Bsz, Dch, N, io = cfg["batch"], cfg["dim"], cfg["dstate"], cfg["io"]
+    dev = torch.device("cuda")
+    A, D, bias, _ = inputs.channel_params(Dch, N, cfg["seed"])
+    A, D, bias = (torch.from_numpy(a).to(dev) for a in (A, D, bias))
+    st0 = torch.from_numpy(inputs.make_decode_state(Bsz, Dch, N, cfg["seed"])).to(dev)
+    nbytes = step_bytes(Bsz, Dch, N, io)
+    R = max(2, math.ceil(3 * L2_BYTES / nbytes))
+    states = [st0.clone() for _ in range(R)]
+    P = 8   # distinct per-step inputs, cycled
+
+    def d(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    steps_in = []
+    for k in range(P):
+        s = inputs.make_decode_step(Bsz, Dch, N, cfg["seed"], k, io)
+        steps_in.append({n: d(getattr(s, n)) for n in ("u", "delta", "z", "B", "C")})
+    ys = [torch.empty((Bsz, Dch), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        s = steps_in[i % P]
+        m.mamba_state_update(states[i % R], s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, ys[i % R],
+                             stream=stream)
+
+    mufu_per_clk, sms = mufu_ex2_per_clk_per_sm(m, torch)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(torch.cuda.current_device()) as cs:
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    t_ms = ev0.elapsed_time(ev1) / args.steps
+
+    hst = states[0].cpu().pin_memory()
+    hin = [{k: v.cpu().pin_memory() for k, v in s.items()} for s in steps_in[:2]]
+    hy = torch.empty((Bsz, Dch), dtype=torch.bfloat16).pin_memory()
+    dst = states[0]
+    dins = steps_in[0]
+
+    def e2e_step(i):
+        dst.copy_(hst, non_blocking=True)
+        for k in dins:
+            dins[k].copy_(hin[i % 2][k], non_blocking=True)
+        m.mamba_state_update(dst, dins["u"], dins["delta"], A, dins["B"], dins["C"], D, dins["z"], bias, 1, ys[0],
+                             stream=stream)
+        hy.copy_(ys[0], non_blocking=True)
+        hst.copy_(dst, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    h2d = hst.numel() * 4 + sum(v.numel() * v.element_size() for v in hin[0].values())
+    d2h = hy.numel() * 2 + hst.numel() * 4
+    peaks = measured_peaks()
+    t_meas = t_ms * 1e-3
+    roof = {"bound": "hbm", "achieved": round(nbytes / t_meas / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(nbytes / (peaks["hbm_gbs"] * 1e9) / t_meas, 4),
+            "traffic": traffic_record(cfg["name"]), "kernel": "state_update_kernel<bf16,NP16>",
+            "peak_source": f"{peaks['source']} copy bandwidth"}
+    return dict(ms_per_step=t_ms, bytes=nbytes, tokens=Bsz, dtype="bf16",
+                config={"workload": cfg["name"], "batch": Bsz, "d_inner": Dch, "d_state": N, "io": io,
+                        "state": "fp32", "l2": f"state rotates over {R} resident copies "
+                                                f"({R * nbytes / 1e6:.0f} MB > L2)"},
+                roofline=roof, h2d=h2d, d2h=d2h, e2e_ms=e2e_ms, launches=args.steps, clocks=cs.summary(),
+                mufu={"ex2_per_clk_per_sm": round(mufu_per_clk, 3), "sms": sms})
+
+
+def reference_arm(args, world, rank):
+    """The oracle (float64, host cores) on a bounded sample of the same workload."""
+    if rank != 0:
+        return
+    if args.workload == inputs.DECODE_WORKLOAD["name"]:
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the scan workloads only"}))
+        return
+    x = inputs.make_workload(args.workload)
+    Bsz, Dch, L, N = x.shape
+    vals = []
+    info = None
+    budget = max(2.0, 60.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        bps, ups, info = time_oracle(x, budget_s=budget)
+        if i >= args.warmup:
+            vals.append(bps)
+    v = statistics.median(vals) / 1e9
+    t_ms = scan_bytes(Bsz, Dch, L, N, x.io) / (v * 1e9) * 1e3
+    line = {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "batch": Bsz, "d_inner": Dch, "d_state": N, "seq_len": L,
+                       "io": x.io},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": info["threads"], "kind": "oracle",
+                             "sample": f"whole time rows of {info['channels']} of {info['of']} channels per step"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

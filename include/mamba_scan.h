@@ -1,0 +1,170 @@
+/*
+ * mamba_scan.h -- C ABI of the B300 (sm_103a) selective-scan library
+ * (libmambascan.so).
+ *
+ * The library computes the selective state-space recurrence of Mamba for every
+ * batch b, channel d and state n:
+ *
+ *   Delta_t = softplus(Delta_raw_t + bias_d)        (or Delta_raw_t + bias_d)
+ *   A_bar_t = exp(Delta_t * A_{d,n})
+ *   h_t     = A_bar_t * h_{t-1} + Delta_t * B_{t,n} * u_t
+ *   y_t     = (sum_n C_{t,n} * h_t + D_d * u_t) * SiLU(z_t)      (gate optional)
+ *
+ * Sources: "Mamba state space model" explainer (fsdata.site) §3.2, the
+ * selective_step function (softplus step size, A_bar = exp(dt*A),
+ * B_bar = dt*B, h = A_bar*h + B_bar*x, y = C.h + D*x); "Mamba: linear-time
+ * sequence modelling with selective state spaces" tutorial (freeguideonline)
+ * §4.2 step 2 (Delta bias inside the softplus), §4.3 (each channel owns an
+ * independent N-wide state), §2.2 (exact zero-order hold), §5.1 (the scan as
+ * an associative combination of step transforms), §4.1 (gate branch);
+ * "Mamba: Linear-Time Sequence Modeling with Selective State Spaces" summary
+ * (ai.xwebgame.com), PyTorch block (the gate is SiLU of the residual branch).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All tensor pointers are DEVICE pointers on the calling thread's current
+ *    CUDA device, owned by the caller.  The library never frees or retains
+ *    them.  Outputs must not alias inputs.
+ *  - Layouts are dense, row-major, innermost dimension last:
+ *        u, delta, z, y     [Bsz][Dch][L]     (time contiguous)
+ *        B, C               [Bsz][N][L]       (shared by every channel of b)
+ *        A                  [Dch][N]  fp32    (real; negative for decay)
+ *        D, delta_bias      [Dch]     fp32
+ *        last_state, h0     [Bsz][Dch][N] fp32
+ *    "dtype" is the storage type of u, delta, z, B, C and y: MAMBA_F32 or
+ *    MAMBA_BF16.  State, A, D and bias are always fp32; arithmetic is fp32.
+ *  - D, z, delta_bias, last_state (and h0) may be NULL: NULL means absent
+ *    (D = 0, no gate, bias = 0, state not written, zero initial state).
+ *  - Calls are asynchronous and ordered on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).  A return of MAMBA_OK means the work was
+ *    enqueued; device-side failures surface at the caller's next
+ *    synchronisation.  Invalid arguments are rejected on the host before any
+ *    CUDA call and nothing is launched.
+ *  - No C++ exception crosses this interface.  Pointers that are not 16-byte
+ *    aligned, or rows whose byte length is not a multiple of 16, select a
+ *    slower scalar-load kernel; they are never an error.
+ */
+#ifndef MAMBA_SCAN_H
+#define MAMBA_SCAN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle; binary-compatible with cudaStream_t. */
+typedef struct CUstream_st *mamba_stream_t;
+
+/* Storage types (the `dtype` argument). */
+enum mamba_dtype { MAMBA_F32 = 0, MAMBA_BF16 = 1 };
+
+/* Status codes. */
+enum mamba_status {
+    MAMBA_OK = 0,
+    MAMBA_ERR_NULL_ARG = -1,        /* a required pointer is NULL */
+    MAMBA_ERR_BAD_SHAPE = -2,       /* a size is <= 0 (or too large to index) */
+    MAMBA_ERR_UNSUPPORTED_N = -3,   /* N > 64 */
+    MAMBA_ERR_BAD_DTYPE = -4,       /* dtype is not MAMBA_F32 / MAMBA_BF16 */
+    MAMBA_ERR_ALLOC = -5,           /* stream-ordered workspace allocation failed */
+    MAMBA_ERR_LAUNCH = -6,          /* a kernel launch failed (cudaGetLastError) */
+    MAMBA_ERR_DEVICE_TIMEOUT = -7,  /* reserved: a bounded device-side wait expired */
+    MAMBA_ERR_BAD_FLAGS = -8,       /* unknown bit in `flags` */
+    MAMBA_ERR_WORKSPACE = -9,       /* caller workspace too small or misaligned */
+    MAMBA_ERR_DEVICE = -10          /* no usable CUDA device / query failed */
+};
+
+/* Flags of mamba_selective_scan_fwd_ex. */
+#define MAMBA_FLAG_ZOH 0x1     /* exact zero-order hold: B_bar = (exp(Delta*A) - 1) / A * B
+                                  (Delta*B where A == 0); freeguideonline tutorial §2.2 */
+#define MAMBA_FLAG_REVERSE 0x2 /* scan t = L-1 down to 0 (the reverse SSM stacked for
+                                  bidirectional context; fsdata.site explainer §7 table) */
+
+/*
+ * Selective scan forward over a whole sequence, zero initial state.
+ *
+ *   u, delta, z  [Bsz][Dch][L]   delta is Delta_raw (before bias/softplus)
+ *   A [Dch][N] fp32, B, C [Bsz][N][L], D [Dch] fp32, delta_bias [Dch] fp32
+ *   softplus_flag  non-zero: Delta = softplus(delta + bias); zero: delta + bias
+ *   y            [Bsz][Dch][L]   output, same dtype as u
+ *   last_state   [Bsz][Dch][N]   fp32 output h_{L-1} (may be NULL)
+ *   Bsz, Dch, L >= 1; 1 <= N <= 64
+ *
+ * When Bsz*Dch is too small to fill the GPU and L is long, the call runs the
+ * sequence-parallel chunked scan (chunk end states, an associative carry over
+ * the chunks, then a seeded rescan); its workspace is allocated and freed
+ * stream-ordered inside the call (cudaMallocAsync / cudaFreeAsync on
+ * `stream`).  Returns MAMBA_OK or a negative mamba_status.
+ */
+int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A, const void *B,
+                             const void *C, const float *D, const void *z, const float *delta_bias,
+                             int softplus_flag, void *y, float *last_state, int64_t Bsz,
+                             int64_t Dch, int64_t L, int64_t N, int dtype, mamba_stream_t stream);
+
+/*
+ * Extended forward scan: everything of mamba_selective_scan_fwd, plus
+ *   h0          [Bsz][Dch][N] fp32 initial state (NULL = zero).  With
+ *               MAMBA_FLAG_REVERSE it is the state "after" t = L, i.e. the
+ *               state the backward-in-time scan starts from.
+ *   flags       MAMBA_FLAG_ZOH | MAMBA_FLAG_REVERSE (0 = plain forward scan)
+ *   chunk_len   0: automatic choice between the direct and the chunked scan;
+ *               > 0: force the chunked scan with chunks of this many steps
+ *                    (rounded up to the kernel's time tile);
+ *               < 0: force the direct (single pass) scan.
+ *   workspace, workspace_bytes
+ *               caller-owned device scratch for the chunked scan (256-byte
+ *               aligned, at least mamba_scan_workspace_size(...) bytes), or
+ *               NULL to let the call allocate it stream-ordered.
+ * Returns MAMBA_ERR_WORKSPACE if a non-NULL workspace is too small or not
+ * 256-byte aligned, MAMBA_ERR_BAD_FLAGS for unknown flag bits.
+ */
+int mamba_selective_scan_fwd_ex(const void *u, const void *delta, const float *A, const void *B,
+                                const void *C, const float *D, const void *z,
+                                const float *delta_bias, int softplus_flag, void *y,
+                                float *last_state, const float *h0, int64_t Bsz, int64_t Dch,
+                                int64_t L, int64_t N, int dtype, int flags, int64_t chunk_len,
+                                void *workspace, size_t workspace_bytes, mamba_stream_t stream);
+
+/*
+ * Bytes of device workspace the scan needs for these sizes and chunk_len (same
+ * meaning as in _ex), on the current device.  0 means the direct scan runs and
+ * needs none.  Returns (size_t)-1 if the sizes are invalid or the device query
+ * fails.
+ */
+size_t mamba_scan_workspace_size(int64_t Bsz, int64_t Dch, int64_t L, int64_t N, int64_t chunk_len,
+                                 int dtype);
+
+/*
+ * One-token recurrent step (selective_state_update) for every (b, d):
+ *   state  [Bsz][Dch][N] fp32, read and overwritten in place with h_t
+ *   u, delta, z, y  [Bsz][Dch];  B, C [Bsz][N];  A [Dch][N] fp32;  D, delta_bias [Dch] fp32
+ *   y = (C . h_t + D*u) * SiLU(z), same dtype as u.
+ * Source: the selective_step function of the fsdata.site explainer §3.2
+ * applied to a stored state (inference carries only the fixed-size state,
+ * same page, §5 table).  D, z, delta_bias may be NULL.  1 <= N <= 64.
+ */
+int mamba_state_update(float *state, const void *u, const void *delta, const float *A,
+                       const void *B, const void *C, const float *D, const void *z,
+                       const float *delta_bias, int softplus_flag, void *y, int64_t Bsz,
+                       int64_t Dch, int64_t N, int dtype, mamba_stream_t stream);
+
+/* Static, human-readable text for a status code (never NULL). */
+const char *mamba_status_string(int status);
+
+/*
+ * Microbenchmark of the special-function (MUFU) pipe: launches `blocks` CTAs
+ * of `threads` threads, each thread running `iters` rounds of 8 independent
+ * ex2.approx.ftz.f32; writes per-CTA elapsed SM clock cycles to
+ * cycles[blocks] (int64, device memory) and a checksum to sink[blocks*threads]
+ * (fp32, device memory) so nothing is optimised away.  Not part of the scan;
+ * it measures the exp throughput that bounds it.
+ */
+int mamba_bench_ex2(int64_t *cycles, float *sink, int64_t iters, int blocks, int threads,
+                    mamba_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MAMBA_SCAN_H */

@@ -1,0 +1,47 @@
+// internal.h -- host-side launch interface between the C ABI (api.cu) and the
+// kernels.  Not installed; the public interface is include/mamba_scan.h.
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "scan_kernels.cuh"
+
+namespace mamba {
+
+constexpr int kMaxDevices = 64;
+
+// Tile geometry of the scan kernel for a padded state count NP (4..64).
+struct ScanGeom {
+    int NP;      // padded state count (power of two >= N, >= 4)
+    int TT;      // time steps per tile; chunk lengths are multiples of it
+    int S;       // lanes per channel
+    int CH;      // channels per CTA
+    int threads; // threads per CTA
+};
+ScanGeom scan_geom(long long N);
+
+// Launch the scan kernel: grid (ceil(Dch/CH), Bsz, grid_chunks).
+cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long long Bsz, int grid_chunks,
+                        cudaStream_t st);
+
+// Carry pass of the chunked scan: per (b, d, n) an exclusive combine over the
+// K chunk (decay, end-state) pairs; writes every chunk's initial state into
+// ws_h in place (hin[k] = prod decay * h0 + ...).
+cudaError_t launch_carry(const float *A, const float *h0, float *ws_h, const float *ws_sdt, long long Bsz,
+                         long long Dch, long long N, int K, cudaStream_t st);
+
+struct StepArgs {
+    float *state;
+    const void *u, *delta, *z, *Bm, *Cm;
+    const float *A, *D, *bias;
+    void *y;
+    long long Bsz, Dch, N;
+    int softplus;
+};
+cudaError_t launch_state_update(int dtype, bool vec, const StepArgs &a, cudaStream_t st);
+
+cudaError_t launch_bench_ex2(long long *cycles, float *sink, long long iters, int blocks, int threads,
+                             cudaStream_t st);
+
+}  // namespace mamba

@@ -1,0 +1,78 @@
+// scan_fwd.cu -- instantiations and launch of the selective-scan kernel.
+#include "internal.h"
+
+namespace mamba {
+
+// Kernel configuration per padded state count.  NS states per lane, NP/NS
+// lanes per channel, NWARPS warps per CTA, TT steps per tile.
+template <int NP>
+struct Cfg;
+template <> struct Cfg<4> { static constexpr int NS = 4, TT = 16, NWARPS = 2; };
+template <> struct Cfg<8> { static constexpr int NS = 4, TT = 16, NWARPS = 2; };
+template <> struct Cfg<16> { static constexpr int NS = 4, TT = 32, NWARPS = 2; };
+template <> struct Cfg<32> { static constexpr int NS = 8, TT = 32, NWARPS = 2; };
+template <> struct Cfg<64> { static constexpr int NS = 16, TT = 32, NWARPS = 2; };
+
+template <int NP>
+static ScanGeom geom_of() {
+    using C = Cfg<NP>;
+    using Sh = ScanShape<NP, C::NS, C::TT, C::NWARPS, MODE_FULL, 2>;
+    return ScanGeom{NP, C::TT, Sh::S, Sh::CH, Sh::NTHR};
+}
+
+ScanGeom scan_geom(long long N) {
+    if (N <= 4) return geom_of<4>();
+    if (N <= 8) return geom_of<8>();
+    if (N <= 16) return geom_of<16>();
+    if (N <= 32) return geom_of<32>();
+    return geom_of<64>();
+}
+
+template <typename T, int NP, int MODE, bool VEC>
+static cudaError_t launch_one(const ScanArgs &a, long long Bsz, int grid_chunks, cudaStream_t st) {
+    using C = Cfg<NP>;
+    using Sh = ScanShape<NP, C::NS, C::TT, C::NWARPS, MODE, (int)sizeof(T)>;
+    auto kern = scan_kernel<T, NP, C::NS, C::TT, C::NWARPS, MODE, VEC>;
+    if (Sh::SMEM_BYTES > 48 * 1024) {
+        // opt in to more than 48 KB of dynamic shared memory, once per device
+        static bool attr_set[kMaxDevices] = {};
+        int dev = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e != cudaSuccess) return e;
+        if (dev < 0 || dev >= kMaxDevices || !attr_set[dev]) {
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM_BYTES);
+            if (e != cudaSuccess) return e;
+            if (dev >= 0 && dev < kMaxDevices) attr_set[dev] = true;
+        }
+    }
+    dim3 grid((unsigned)((a.Dch + Sh::CH - 1) / Sh::CH), (unsigned)Bsz, (unsigned)grid_chunks);
+    kern<<<grid, Sh::NTHR, Sh::SMEM_BYTES, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T, int NP>
+static cudaError_t launch_np(int mode, bool vec, const ScanArgs &a, long long Bsz, int gc, cudaStream_t st) {
+    if (mode == MODE_FULL)
+        return vec ? launch_one<T, NP, MODE_FULL, true>(a, Bsz, gc, st) : launch_one<T, NP, MODE_FULL, false>(a, Bsz, gc, st);
+    return vec ? launch_one<T, NP, MODE_STATES, true>(a, Bsz, gc, st) : launch_one<T, NP, MODE_STATES, false>(a, Bsz, gc, st);
+}
+
+template <typename T>
+static cudaError_t launch_t(int mode, bool vec, const ScanArgs &a, long long Bsz, int gc, cudaStream_t st) {
+    const int NP = scan_geom(a.N).NP;
+    switch (NP) {
+        case 4: return launch_np<T, 4>(mode, vec, a, Bsz, gc, st);
+        case 8: return launch_np<T, 8>(mode, vec, a, Bsz, gc, st);
+        case 16: return launch_np<T, 16>(mode, vec, a, Bsz, gc, st);
+        case 32: return launch_np<T, 32>(mode, vec, a, Bsz, gc, st);
+        default: return launch_np<T, 64>(mode, vec, a, Bsz, gc, st);
+    }
+}
+
+cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long long Bsz, int grid_chunks,
+                        cudaStream_t st) {
+    return dtype == 1 ? launch_t<bf16_t>(mode, vec, a, Bsz, grid_chunks, st)
+                      : launch_t<float>(mode, vec, a, Bsz, grid_chunks, st);
+}
+
+}  // namespace mamba

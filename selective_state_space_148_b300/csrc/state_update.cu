@@ -1,0 +1,106 @@
+// state_update.cu -- one-token recurrent step (selective_state_update).
+//
+// The selective_step of the fsdata.site explainer §3.2 applied to a stored
+// state: Delta = softplus(Delta_raw + bias), h = exp(Delta A) h + Delta B u,
+// y = (C . h + D u) * SiLU(z).  The state [Bsz][Dch][N] fp32 is read and
+// written once per call, so the kernel is bound by HBM bandwidth on the state
+// bytes: every thread owns 4 consecutive states of one (b, d) and moves them
+// with one 16-byte load and one 16-byte store; the NP/4 lanes of a (b, d)
+// reduce C . h with butterfly shuffles and the first of them writes y.
+#include "internal.h"
+
+namespace mamba {
+
+template <typename T, int NP, bool VEC>
+__global__ void __launch_bounds__(256)
+state_update_kernel(const StepArgs a) {
+    using IO = Io<T>;
+    constexpr int G = NP / 4;  // lanes per (b, d)
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long ch = gid / G;  // b * Dch + d
+    const int q = (int)(gid % G);
+    const long long nch = a.Bsz * a.Dch;
+    const bool valid = ch < nch;
+    const long long cc = valid ? ch : 0;
+    const long long b = cc / a.Dch, d = cc % a.Dch;
+    const long long N = a.N;
+    const long long n0 = 4LL * q;
+
+    float h[4] = {0.f, 0.f, 0.f, 0.f}, A2[4] = {0.f, 0.f, 0.f, 0.f};
+    float Bv[4] = {0.f, 0.f, 0.f, 0.f}, Cv[4] = {0.f, 0.f, 0.f, 0.f};
+    if (valid) {
+        if (VEC && n0 < N) {  // N % 4 == 0 and 16-byte aligned rows
+            const float4 hv = __ldcs(reinterpret_cast<const float4 *>(a.state + cc * N + n0));
+            const float4 av = __ldg(reinterpret_cast<const float4 *>(a.A + d * N + n0));
+            h[0] = hv.x; h[1] = hv.y; h[2] = hv.z; h[3] = hv.w;
+            A2[0] = av.x; A2[1] = av.y; A2[2] = av.z; A2[3] = av.w;
+        } else {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                if (n0 + j < N) {
+                    h[j] = a.state[cc * N + n0 + j];
+                    A2[j] = a.A[d * N + n0 + j];
+                }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            A2[j] *= kLog2e;
+            if (n0 + j < N) {
+                Bv[j] = IO::load(a.Bm, b * N + n0 + j);
+                Cv[j] = IO::load(a.Cm, b * N + n0 + j);
+            }
+        }
+    }
+    const float uu = valid ? IO::load(a.u, cc) : 0.f;
+    const float raw = (valid ? IO::load(a.delta, cc) : 0.f) + (a.bias != nullptr && valid ? a.bias[d] : 0.f);
+    const float dl = a.softplus ? softplus_f(raw) : raw;
+    const float du = dl * uu;
+    float p = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * Bv[j]);
+        p = fmaf(Cv[j], h[j], p);
+    }
+#pragma unroll
+    for (int off = 1; off < G; off <<= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+    if (!valid) return;
+    if (VEC && n0 < N) {
+        __stcs(reinterpret_cast<float4 *>(a.state + cc * N + n0), make_float4(h[0], h[1], h[2], h[3]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            if (n0 + j < N) a.state[cc * N + n0 + j] = h[j];
+    }
+    if (q == 0) {
+        float y = fmaf(a.D != nullptr ? a.D[d] : 0.f, uu, p);
+        if (a.z != nullptr) y *= silu_f(IO::load(a.z, cc));
+        IO::store(a.y, cc, y);
+    }
+}
+
+template <typename T, int NP>
+static cudaError_t launch_np(bool vec, const StepArgs &a, cudaStream_t st) {
+    const long long total = a.Bsz * a.Dch * (NP / 4);
+    const int threads = 256;
+    const long long blocks = (total + threads - 1) / threads;
+    if (vec)
+        state_update_kernel<T, NP, true><<<(unsigned)blocks, threads, 0, st>>>(a);
+    else
+        state_update_kernel<T, NP, false><<<(unsigned)blocks, threads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename T>
+static cudaError_t launch_t(bool vec, const StepArgs &a, cudaStream_t st) {
+    if (a.N <= 4) return launch_np<T, 4>(vec, a, st);
+    if (a.N <= 8) return launch_np<T, 8>(vec, a, st);
+    if (a.N <= 16) return launch_np<T, 16>(vec, a, st);
+    if (a.N <= 32) return launch_np<T, 32>(vec, a, st);
+    return launch_np<T, 64>(vec, a, st);
+}
+
+cudaError_t launch_state_update(int dtype, bool vec, const StepArgs &a, cudaStream_t st) {
+    return dtype == 1 ? launch_t<bf16_t>(vec, a, st) : launch_t<float>(vec, a, st);
+}
+
+}  // namespace mamba

@@ -1,0 +1,72 @@
+"""Shared test helpers: host <-> device conversion of the generator's arrays and
+the tolerance check.  No scan arithmetic here."""
+import numpy as np
+
+from selective_state_space_148_b300 import inputs
+
+# Tolerances (elementwise, |gpu - oracle| <= tol * (1 + |oracle|)):
+TOL_Y = {"f32": 1e-4, "bf16": 2e-2}   # y for fp32 / bf16 storage
+TOL_STATE = 1e-4                      # fp32 last_state of a scan
+TOL_STATE_CHAIN = 1e-3                # fp32 state after a long chain of decode steps
+
+
+def to_dev(arr, io, device="cuda"):
+    """Generator array (bf16 bits or fp32) -> torch tensor on the GPU with the storage dtype."""
+    import torch
+    if arr is None:
+        return None
+    if io == "bf16":
+        return torch.from_numpy(np.ascontiguousarray(arr).view(np.int16)).to(device).view(torch.bfloat16)
+    return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32)).to(device)
+
+
+def f32_dev(arr, device="cuda"):
+    import torch
+    if arr is None:
+        return None
+    return torch.from_numpy(np.ascontiguousarray(arr, dtype=np.float32)).to(device)
+
+
+def to_host_f64(t):
+    """GPU tensor (fp32 or bf16) -> float64 numpy array, exact."""
+    import torch
+    if t.dtype == torch.bfloat16:
+        return inputs.to_f64(t.view(torch.int16).cpu().numpy().view(np.uint16), "bf16")
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def rel_err(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if got.size == 0:
+        return 0.0
+    return float(np.max(np.abs(got - ref) / (1.0 + np.abs(ref))))
+
+
+def assert_close(got, ref, tol, what=""):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    e = rel_err(got, ref)
+    assert e <= tol, f"{what}: max |err|/(1+|ref|) = {e:.3g} > {tol}"
+    return e
+
+
+def dev_inputs(x: "inputs.ScanInputs"):
+    """All scan inputs of a ScanInputs on the GPU."""
+    return dict(u=to_dev(x.u, x.io), delta=to_dev(x.delta, x.io), z=to_dev(x.z, x.io), B=to_dev(x.B, x.io),
+                C=to_dev(x.C, x.io), A=f32_dev(x.A), D=f32_dev(x.D), delta_bias=f32_dev(x.delta_bias))
+
+
+def oracle_rows(x: "inputs.ScanInputs", chans, softplus=True, h0=None, disc=0, reverse=False, with_z=True):
+    """Oracle y and last_state for a list of (b, d) channels only."""
+    import oracle
+    ys, hs = [], []
+    for (b, d) in chans:
+        sl = lambda a: None if a is None else inputs.to_f64(a[b:b + 1, d:d + 1], x.io)
+        y, h = oracle.selective_scan(sl(x.u), sl(x.delta), x.A[d:d + 1].astype(np.float64),
+                                     inputs.to_f64(x.B[b:b + 1], x.io), inputs.to_f64(x.C[b:b + 1], x.io),
+                                     x.D[d:d + 1].astype(np.float64), sl(x.z) if with_z else None,
+                                     x.delta_bias[d:d + 1].astype(np.float64), softplus_flag=softplus,
+                                     h0=None if h0 is None else h0[b:b + 1, d:d + 1], disc=disc, reverse=reverse)
+        ys.append(y[0, 0])
+        hs.append(h[0, 0])
+    return np.stack(ys), np.stack(hs)

@@ -1,0 +1,243 @@
+"""Parity of the CUDA selective scan (through the C ABI) with the float64 oracle.
+
+Small and mid sizes are compared element by element on every output; the full
+workload sizes are compared on sampled channels (whole time rows and final
+states), which the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import selective_state_space_148_b300 as m
+from selective_state_space_148_b300 import inputs
+from helpers import (TOL_STATE, TOL_Y, assert_close, dev_inputs, f32_dev, oracle_rows, to_dev, to_host_f64)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_gpu(x, softplus=True, with_z=True, with_D=True, with_bias=True, h0=None, chunk_len=0, flags=0,
+            want_last=True):
+    import torch
+    t = dev_inputs(x)
+    y = torch.empty_like(t["u"])
+    last = torch.empty((x.shape[0], x.shape[1], x.shape[3]), dtype=torch.float32, device="cuda") if want_last else None
+    h0d = f32_dev(h0)
+    if h0 is None and chunk_len == 0 and flags == 0:
+        m.mamba_selective_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"] if with_D else None,
+                                   t["z"] if with_z else None, t["delta_bias"] if with_bias else None, softplus, y,
+                                   last)
+    else:
+        m.mamba_selective_scan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"] if with_D else None,
+                                      t["z"] if with_z else None, t["delta_bias"] if with_bias else None, softplus,
+                                      y, last, h0=h0d, flags=flags, chunk_len=chunk_len)
+    torch.cuda.synchronize()
+    return to_host_f64(y), (last.cpu().numpy().astype(np.float64) if want_last else None)
+
+
+def run_oracle(x, softplus=True, with_z=True, with_D=True, with_bias=True, h0=None, disc=0, reverse=False):
+    return oracle.selective_scan(x.f64("u"), x.f64("delta"), x.f64("A"), x.f64("B"), x.f64("C"),
+                                 x.f64("D") if with_D else None, x.f64("z") if with_z else None,
+                                 x.f64("delta_bias") if with_bias else None, softplus_flag=softplus, h0=h0,
+                                 disc=disc, reverse=reverse)
+
+
+def check(x, tag, **kw):
+    okw = {k: v for k, v in kw.items() if k in ("softplus", "with_z", "with_D", "with_bias", "h0")}
+    yg, hg = run_gpu(x, **kw)
+    yr, hr = run_oracle(x, **okw)
+    ey = assert_close(yg, yr, TOL_Y[x.io], f"{tag} y")
+    eh = assert_close(hg, hr, TOL_STATE, f"{tag} last_state")
+    return ey, eh
+
+
+# ----------------------------------------------------------------------------- workloads, whole outputs
+
+def test_tiny_fp32_workload():
+    x = inputs.make_workload("tiny_b1_d64_n16_l256_f32")
+    ey, eh = check(x, "tiny")
+    print(f"tiny fp32: max y err ratio {ey:.3g}, state {eh:.3g}")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("L", [1, 7, 8, 9, 31, 33, 63, 65, 257, 1000])
+def test_lengths(io, L):
+    x = inputs.make_scan_inputs(2, 37, 16, L, io=io, seed=7)
+    check(x, f"L={L} {io}")
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 12, 16, 17, 24, 32, 33, 48, 64])
+def test_state_sizes(N):
+    x = inputs.make_scan_inputs(2, 19, N, 130, io="bf16", seed=8)
+    check(x, f"N={N}")
+    x = inputs.make_scan_inputs(1, 9, N, 77, io="f32", seed=9)
+    check(x, f"N={N} f32")
+
+
+@pytest.mark.parametrize("variant", ["no_softplus", "no_z", "no_D", "no_bias", "nothing_optional"])
+def test_optional_inputs(variant):
+    x = inputs.make_scan_inputs(2, 40, 16, 200, io="bf16", seed=10)
+    kw = dict(softplus=variant != "no_softplus", with_z=variant not in ("no_z", "nothing_optional"),
+              with_D=variant not in ("no_D", "nothing_optional"), with_bias=variant not in ("no_bias", "nothing_optional"))
+    if variant == "no_softplus":
+        # Delta = Delta_raw + bias must stay positive for a decaying state: shift the raw values up
+        x.delta_bias = (x.delta_bias * 0 + 2.0).astype(np.float32)
+    check(x, variant, **kw)
+
+
+def test_no_last_state():
+    x = inputs.make_scan_inputs(2, 20, 16, 100, io="bf16", seed=11)
+    yg, _ = run_gpu(x, want_last=False)
+    yr, _ = run_oracle(x)
+    assert_close(yg, yr, TOL_Y["bf16"], "y without last_state")
+
+
+def test_mid_bf16_several_tiles():
+    x = inputs.make_scan_inputs(3, 100, 16, 1000, io="bf16", seed=12)
+    ey, eh = check(x, "mid bf16")
+    print(f"mid bf16: y err ratio {ey:.3g}, state {eh:.3g}")
+
+
+def test_initial_state_direct():
+    x = inputs.make_scan_inputs(2, 33, 16, 150, io="f32", seed=13)
+    h0 = np.random.default_rng(1).normal(0, 0.5, (2, 33, 16)).astype(np.float32).astype(np.float64)
+    check(x, "h0 direct", h0=h0, chunk_len=-1)
+
+
+# ----------------------------------------------------------------------------- chunked scan
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("chunk_len", [32, 64, 96, 160, 1024])
+def test_chunked_forced(io, chunk_len):
+    x = inputs.make_scan_inputs(2, 24, 16, 999, io=io, seed=14)
+    check(x, f"chunked {chunk_len} {io}", chunk_len=chunk_len)
+
+
+@pytest.mark.parametrize("N", [4, 16, 33, 64])
+def test_chunked_state_sizes(N):
+    x = inputs.make_scan_inputs(1, 20, N, 700, io="bf16", seed=15)
+    check(x, f"chunked N={N}", chunk_len=64)
+
+
+def test_chunked_with_initial_state():
+    x = inputs.make_scan_inputs(2, 24, 16, 500, io="f32", seed=16)
+    h0 = np.random.default_rng(2).normal(0, 0.5, (2, 24, 16)).astype(np.float32).astype(np.float64)
+    check(x, "chunked h0", h0=h0, chunk_len=64)
+
+
+def test_chunked_equals_direct_bits_close():
+    """Forced chunked scans agree with the direct scan for several chunk counts."""
+    x = inputs.make_scan_inputs(1, 64, 16, 4096, io="bf16", seed=17)
+    y0, h0 = run_gpu(x, chunk_len=-1)
+    for cl in (32, 128, 1000, 4096):
+        y1, h1 = run_gpu(x, chunk_len=cl)
+        assert_close(y1, y0, TOL_Y["bf16"], f"chunk {cl} vs direct y")
+        assert_close(h1, h0, TOL_STATE, f"chunk {cl} vs direct state")
+
+
+def test_automatic_choice_uses_chunks_for_long_thin_problems():
+    # one channel block and a long sequence: the automatic plan cuts it into chunks
+    assert m.mamba_scan_workspace_size(1, 16, 1 << 16, 16, 0, m.MAMBA_BF16) > 0
+    # a wide problem stays direct
+    assert m.mamba_scan_workspace_size(8, 1536, 2048, 16, 0, m.MAMBA_BF16) == 0
+    x = inputs.make_scan_inputs(1, 16, 16, 1 << 14, io="bf16", seed=18)
+    check(x, "auto chunked")
+
+
+# ----------------------------------------------------------------------------- memory safety and errors
+
+def test_guard_regions_untouched():
+    """Outputs written through views inside larger buffers: the guard elements keep their sentinel."""
+    import torch
+    x = inputs.make_scan_inputs(2, 21, 16, 77, io="bf16", seed=19)
+    t = dev_inputs(x)
+    G = 64
+    ybuf = torch.full((2 * 21 * 77 + 2 * G,), -12345.0, dtype=torch.float32, device="cuda").to(torch.bfloat16)
+    hbuf = torch.full((2 * 21 * 16 + 2 * G,), -777.0, dtype=torch.float32, device="cuda")
+    y = ybuf[G:G + 2 * 21 * 77].view(2, 21, 77)
+    h = hbuf[G:G + 2 * 21 * 16].view(2, 21, 16)
+    m.mamba_selective_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], 1, y, h)
+    torch.cuda.synchronize()
+    assert torch.all(ybuf[:G].float() == -12345.0) and torch.all(ybuf[-G:].float() == -12345.0)
+    assert torch.all(hbuf[:G] == -777.0) and torch.all(hbuf[-G:] == -777.0)
+    yr, hr = run_oracle(x)
+    assert_close(to_host_f64(y), yr, TOL_Y["bf16"], "guarded y")
+    assert_close(h.cpu().numpy(), hr, TOL_STATE, "guarded state")
+
+
+def test_misaligned_pointers_take_scalar_path():
+    import torch
+    x = inputs.make_scan_inputs(2, 18, 16, 64, io="bf16", seed=20)
+    t = dev_inputs(x)
+    off = {}
+    for k in ("u", "delta", "z", "B", "C"):   # copy into a buffer shifted by one element
+        buf = torch.empty(t[k].numel() + 1, dtype=t[k].dtype, device="cuda")
+        buf[1:].copy_(t[k].reshape(-1))
+        off[k] = buf[1:].view(t[k].shape)
+    y = torch.empty(t["u"].numel() + 1, dtype=torch.bfloat16, device="cuda")[1:].view(t["u"].shape)
+    h = torch.empty((2, 18, 16), dtype=torch.float32, device="cuda")
+    m.mamba_selective_scan_fwd(off["u"], off["delta"], t["A"], off["B"], off["C"], t["D"], off["z"],
+                               t["delta_bias"], 1, y, h)
+    torch.cuda.synchronize()
+    yr, hr = run_oracle(x)
+    assert_close(to_host_f64(y), yr, TOL_Y["bf16"], "misaligned y")
+    assert_close(h.cpu().numpy(), hr, TOL_STATE, "misaligned state")
+
+
+def test_caller_workspace_and_errors(monkeypatch):
+    import torch
+    x = inputs.make_scan_inputs(1, 16, 16, 2048, io="bf16", seed=21)
+    t = dev_inputs(x)
+    need = m.mamba_scan_workspace_size(1, 16, 2048, 16, 128, m.MAMBA_BF16)
+    assert need > 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    y = torch.empty_like(t["u"])
+    h = torch.empty((1, 16, 16), dtype=torch.float32, device="cuda")
+    m.mamba_selective_scan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], 1, y,
+                                  h, chunk_len=128, workspace=ws, workspace_bytes=need)
+    torch.cuda.synchronize()
+    yr, hr = run_oracle(x)
+    assert_close(to_host_f64(y), yr, TOL_Y["bf16"], "caller workspace y")
+    with pytest.raises(m.MambaError) as ei:
+        m.mamba_selective_scan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"],
+                                      1, y, h, chunk_len=128, workspace=ws, workspace_bytes=need - 4)
+    assert ei.value.status == -9
+    monkeypatch.setenv("MAMBA_FAULT_INJECT", "alloc")
+    with pytest.raises(m.MambaError) as ei:
+        m.mamba_selective_scan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"],
+                                      1, y, h, chunk_len=128)
+    assert ei.value.status == -5
+    # the direct path allocates nothing and is unaffected
+    m.mamba_selective_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], 1, y, h)
+    torch.cuda.synchronize()
+
+
+# ----------------------------------------------------------------------------- full-size workloads, sampled
+
+def sample_channels(Bsz, Dch, k=10, seed=123):
+    rng = np.random.default_rng(seed)
+    ch = {(0, 0), (Bsz - 1, Dch - 1), (Bsz - 1, 0), (0, Dch - 1)}
+    while len(ch) < k:
+        ch.add((int(rng.integers(Bsz)), int(rng.integers(Dch))))
+    return sorted(ch)
+
+
+@pytest.mark.parametrize("name", ["mamba130m_b8_d1536_n16_l2048_bf16", "mamba2p8b_b4_d5120_n16_l4096_bf16",
+                                  "mamba2p8b_b4_d5120_n64_l4096_bf16", "dna_b1_d1536_n16_l1048576_bf16"])
+def test_full_workload_sampled(name):
+    import torch
+    x = inputs.make_workload(name)
+    Bsz, Dch, L, N = x.shape
+    t = dev_inputs(x)
+    y = torch.empty_like(t["u"])
+    h = torch.empty((Bsz, Dch, N), dtype=torch.float32, device="cuda")
+    m.mamba_selective_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], 1, y, h)
+    torch.cuda.synchronize()
+    chans = sample_channels(Bsz, Dch, k=6 if L > 100000 else 12)
+    yr, hr = oracle_rows(x, chans)
+    yg = np.stack([to_host_f64(y[b, d]) for (b, d) in chans])
+    hg = np.stack([h[b, d].cpu().numpy() for (b, d) in chans]).astype(np.float64)
+    ey = assert_close(yg, yr, TOL_Y["bf16"], f"{name} y")
+    eh = assert_close(hg, hr, TOL_STATE, f"{name} state")
+    # properties that hold everywhere: finite outputs
+    assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
+    print(f"{name}: y err ratio {ey:.3g}, state {eh:.3g}, chunked={m.mamba_scan_workspace_size(Bsz, Dch, L, N) > 0}")
