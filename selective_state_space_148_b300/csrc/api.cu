@@ -83,7 +83,7 @@ int make_plan(long long Bsz, long long Dch, long long L, long long N, long long 
         if (st != MAMBA_OK) return st;
         const long long lanes = Bsz * Dch * g.S;
         const long long target = (long long)sms * 1024;  // lanes the GPU can keep in flight
-        if (lanes * 3 >= target || L < 16LL * g.TT) {
+        if (lanes * 4 >= target || L < 16LL * g.TT) {
             *plan = Plan{L, 1};
             return MAMBA_OK;
         }

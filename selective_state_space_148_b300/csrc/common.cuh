@@ -29,6 +29,13 @@ __device__ __forceinline__ float rcp_approx(float x) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float2 f2(float a, float b) { return make_float2(a, b); }
 
 // softplus(x) = log(1 + e^x), for Delta = softplus(Delta_raw + bias)
 // (fsdata.site explainer §3.2; freeguideonline tutorial §4.2 step 2).
@@ -55,6 +62,37 @@ __device__ __forceinline__ float softplus_f(float x) {
 // For z -> -inf, e^-z -> inf and the result tends to -0 as it should.
 __device__ __forceinline__ float silu_f(float z) {
     return z * rcp_approx(1.0f + ex2_approx(-z * kLog2e));
+}
+
+// Pairwise forms used by the scan kernel (two time steps at a time, f32x2).
+// FAST selects the forms used for bf16 storage, whose output rounding (2^-9
+// relative) dwarfs their error:
+//   softplus(x) = max(x, ln2 * log2(1 + 2^(min(x, 15) * log2 e)))  -- two MUFU ops;
+//     the lg2 of a value near 1 carries ~2^-22 absolute error, i.e. ~1e-4
+//     relative error on the smallest Delta of the workloads;
+//   y * SiLU(z) = (y z / 2) (1 + tanh(z / 2))                        -- one MUFU op;
+//     tanh.approx has ~2^-11 relative error.
+// The fp32-storage path keeps the accurate scalar forms above.
+template <bool FAST>
+__device__ __forceinline__ float2 softplus2(float2 x) {
+    if (FAST) {
+        const float2 xm = f2(fminf(x.x, 15.0f), fminf(x.y, 15.0f));
+        const float2 sc = __fmul2_rn(xm, f2(kLog2e, kLog2e));
+        const float2 e1 = __fadd2_rn(f2(ex2_approx(sc.x), ex2_approx(sc.y)), f2(1.0f, 1.0f));
+        const float2 r = __fmul2_rn(f2(lg2_approx(e1.x), lg2_approx(e1.y)), f2(kLn2, kLn2));
+        return f2(fmaxf(r.x, x.x), fmaxf(r.y, x.y));
+    }
+    return f2(softplus_f(x.x), softplus_f(x.y));
+}
+template <bool FAST>
+__device__ __forceinline__ float2 gate2(float2 y, float2 z) {
+    if (FAST) {
+        const float2 g = __fmul2_rn(z, f2(0.5f, 0.5f));
+        const float2 th = f2(tanh_approx(g.x), tanh_approx(g.y));
+        const float2 yg = __fmul2_rn(y, g);
+        return __ffma2_rn(yg, th, yg);
+    }
+    return f2(y.x * silu_f(z.x), y.y * silu_f(z.y));
 }
 
 // ---------------------------------------------------------------- storage types

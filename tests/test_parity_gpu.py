@@ -152,12 +152,13 @@ def test_guard_regions_untouched():
     t = dev_inputs(x)
     G = 64
     ybuf = torch.full((2 * 21 * 77 + 2 * G,), -12345.0, dtype=torch.float32, device="cuda").to(torch.bfloat16)
+    sentinel = float(ybuf[0].float())          # -12345 rounded to bf16
     hbuf = torch.full((2 * 21 * 16 + 2 * G,), -777.0, dtype=torch.float32, device="cuda")
     y = ybuf[G:G + 2 * 21 * 77].view(2, 21, 77)
     h = hbuf[G:G + 2 * 21 * 16].view(2, 21, 16)
     m.mamba_selective_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], 1, y, h)
     torch.cuda.synchronize()
-    assert torch.all(ybuf[:G].float() == -12345.0) and torch.all(ybuf[-G:].float() == -12345.0)
+    assert torch.all(ybuf[:G].float() == sentinel) and torch.all(ybuf[-G:].float() == sentinel)
     assert torch.all(hbuf[:G] == -777.0) and torch.all(hbuf[-G:] == -777.0)
     yr, hr = run_oracle(x)
     assert_close(to_host_f64(y), yr, TOL_Y["bf16"], "guarded y")
@@ -207,8 +208,10 @@ def test_caller_workspace_and_errors(monkeypatch):
                                       1, y, h, chunk_len=128)
     assert ei.value.status == -5
     # the direct path allocates nothing and is unaffected
-    m.mamba_selective_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], 1, y, h)
+    m.mamba_selective_scan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], 1, y,
+                                  h, chunk_len=-1)
     torch.cuda.synchronize()
+    assert_close(to_host_f64(y), yr, TOL_Y["bf16"], "direct y under injected allocation failure")
 
 
 # ----------------------------------------------------------------------------- full-size workloads, sampled
