@@ -72,7 +72,9 @@ enum mamba_status {
     MAMBA_ERR_DEVICE_TIMEOUT = -7,  /* reserved: a bounded device-side wait expired */
     MAMBA_ERR_BAD_FLAGS = -8,       /* unknown bit in `flags` */
     MAMBA_ERR_WORKSPACE = -9,       /* caller workspace too small or misaligned */
-    MAMBA_ERR_DEVICE = -10          /* no usable CUDA device / query failed */
+    MAMBA_ERR_DEVICE = -10,         /* no usable CUDA device / query failed */
+    MAMBA_ERR_SCRATCH_LIMIT = -11   /* mamba_selective_scan_fwd_noalloc: the sizes need more
+                                       scratch than MAMBA_NOALLOC_SCRATCH_BYTES */
 };
 
 /* Flags of mamba_selective_scan_fwd_ex. */
@@ -148,6 +150,41 @@ int mamba_state_update(float *state, const void *u, const void *delta, const flo
                        const void *B, const void *C, const float *D, const void *z,
                        const float *delta_bias, int softplus_flag, void *y, int64_t Bsz,
                        int64_t Dch, int64_t N, int dtype, mamba_stream_t stream);
+
+/*
+ * Chunked forward scan that allocates no device memory (no counterpart in the
+ * pages: this is a deployment variant of the chunked scan above).
+ *
+ * For callers that cannot allocate device memory while they run the scan --
+ * a framework that owns every byte of device memory and hands over only the
+ * tensors of the call, or host code under a fixed memory budget that must
+ * not call (or synchronise with) the allocator.  The caller still provides
+ * every input and output; the chunk end states and step sums live in one
+ * file-scope __device__ array of MAMBA_NOALLOC_SCRATCH_BYTES bytes, which
+ * every GPU that loads the library holds until the process exits.
+ *
+ * Arguments are those of mamba_selective_scan_fwd_ex without flags and
+ * workspace; chunk_len must be >= 1 (rounded up to the kernel's time tile).
+ * When one chunk covers the sequence the direct scan runs and no scratch is
+ * touched.  Needs Bsz*K*Dch*(N+1)*4 bytes (each part rounded up to 256), K =
+ * ceil(L / chunk_len); larger problems return MAMBA_ERR_SCRATCH_LIMIT before
+ * anything is launched.  No cudaMalloc/cudaFree or allocating library call
+ * is made.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  Every call shares the one array and it keeps the
+ * last call's contents (nothing in it needs to start at zero): calls that
+ * overlap on the GPU -- on different streams, or from several host threads --
+ * race on it, so order them on one stream.
+ */
+#define MAMBA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int mamba_selective_scan_fwd_noalloc(const void *u, const void *delta, const float *A, const void *B,
+                                     const void *C, const float *D, const void *z,
+                                     const float *delta_bias, int softplus_flag, void *y,
+                                     float *last_state, const float *h0, int64_t Bsz, int64_t Dch,
+                                     int64_t L, int64_t N, int dtype, int64_t chunk_len,
+                                     mamba_stream_t stream);
 
 /* Static, human-readable text for a status code (never NULL). */
 const char *mamba_status_string(int status);

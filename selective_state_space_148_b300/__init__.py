@@ -25,8 +25,9 @@ MAMBA_FLAG_REVERSE = 0x2
 STATUS = {
     0: "MAMBA_OK", -1: "MAMBA_ERR_NULL_ARG", -2: "MAMBA_ERR_BAD_SHAPE", -3: "MAMBA_ERR_UNSUPPORTED_N",
     -4: "MAMBA_ERR_BAD_DTYPE", -5: "MAMBA_ERR_ALLOC", -6: "MAMBA_ERR_LAUNCH", -7: "MAMBA_ERR_DEVICE_TIMEOUT",
-    -8: "MAMBA_ERR_BAD_FLAGS", -9: "MAMBA_ERR_WORKSPACE", -10: "MAMBA_ERR_DEVICE",
+    -8: "MAMBA_ERR_BAD_FLAGS", -9: "MAMBA_ERR_WORKSPACE", -10: "MAMBA_ERR_DEVICE", -11: "MAMBA_ERR_SCRATCH_LIMIT",
 }
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lib = None
 
@@ -50,6 +51,9 @@ def lib() -> ctypes.CDLL:
         L.mamba_selective_scan_fwd_ex.restype = ci
         L.mamba_selective_scan_fwd_ex.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, vp, vp, vp, i64, i64, i64, i64,
                                                   ci, ci, i64, vp, sz, vp]
+        L.mamba_selective_scan_fwd_noalloc.restype = ci
+        L.mamba_selective_scan_fwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, ci, vp, vp, vp, i64, i64, i64,
+                                                       i64, ci, i64, vp]
         L.mamba_scan_workspace_size.restype = sz
         L.mamba_scan_workspace_size.argtypes = [i64, i64, i64, i64, i64, ci]
         L.mamba_state_update.restype = ci
@@ -119,6 +123,18 @@ def mamba_selective_scan_fwd_ex(u, delta, A, B, C, D, z, delta_bias, softplus_fl
                                            _ptr(h0), Bsz, Dch, L, N, _dtype_code(u), int(flags), int(chunk_len),
                                            _ptr(workspace), int(workspace_bytes), _stream(stream))
     _check(st, "mamba_selective_scan_fwd_ex")
+
+
+def mamba_selective_scan_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, h0=None,
+                                     chunk_len=256, stream=None):
+    """Chunked scan whose scratch is the library's static device array (no device allocation)."""
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    st = lib().mamba_selective_scan_fwd_noalloc(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                                _ptr(delta_bias), int(bool(softplus_flag)), _ptr(y), _ptr(last_state),
+                                                _ptr(h0), Bsz, Dch, L, N, _dtype_code(u), int(chunk_len),
+                                                _stream(stream))
+    _check(st, "mamba_selective_scan_fwd_noalloc")
 
 
 def mamba_scan_workspace_size(Bsz, Dch, L, N, chunk_len=0, dtype=MAMBA_BF16) -> int:

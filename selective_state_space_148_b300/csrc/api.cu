@@ -257,6 +257,7 @@ const char *mamba_status_string(int status) {
         case MAMBA_ERR_BAD_FLAGS: return "unknown or unsupported flag bits";
         case MAMBA_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
         case MAMBA_ERR_DEVICE: return "no usable CUDA device";
+        case MAMBA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the no-allocation entry point holds";
         default: return "unknown status";
     }
 }
