@@ -186,6 +186,14 @@ int mamba_selective_scan_fwd_noalloc(const void *u, const void *delta, const flo
                                      int64_t L, int64_t N, int dtype, int64_t chunk_len,
                                      mamba_stream_t stream);
 
+/*
+ * Reads and clears the library's device error word on the current device
+ * (synchronous).  Returns MAMBA_ERR_DEVICE_TIMEOUT if a bounded device-side
+ * wait of an earlier kernel gave up (that kernel's outputs are then invalid),
+ * MAMBA_OK otherwise, MAMBA_ERR_DEVICE if the query fails.
+ */
+int mamba_device_error(void);
+
 /* Static, human-readable text for a status code (never NULL). */
 const char *mamba_status_string(int status);
 

@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.mamba_state_update.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, vp, i64, i64, i64, ci, vp]
         L.mamba_status_string.restype = ctypes.c_char_p
         L.mamba_status_string.argtypes = [ci]
+        L.mamba_device_error.restype = ci
+        L.mamba_device_error.argtypes = []
         L.mamba_bench_ex2.restype = ci
         L.mamba_bench_ex2.argtypes = [vp, vp, i64, ci, ci, vp]
         _lib = L
@@ -151,6 +153,11 @@ def mamba_state_update(state, u, delta, A, B, C, D, z, delta_bias, softplus_flag
                                   _ptr(delta_bias), int(bool(softplus_flag)), _ptr(y), Bsz, Dch, N,
                                   _dtype_code(u), _stream(stream))
     _check(st, "mamba_state_update")
+
+
+def mamba_device_error() -> int:
+    """Read and clear the device error word (MAMBA_OK or MAMBA_ERR_DEVICE_TIMEOUT)."""
+    return lib().mamba_device_error()
 
 
 def mamba_bench_ex2(cycles, sink, iters, blocks, threads, stream=None):

@@ -25,6 +25,10 @@ ScanGeom scan_geom(long long N);
 cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long long Bsz, int grid_chunks,
                         cudaStream_t st);
 
+// Tensor-memory variant of the scan kernel (N <= 16, 16-byte aligned rows):
+// B/C reach the registers through TMEM instead of shared memory.
+cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &a, long long Bsz, int grid_chunks, cudaStream_t st);
+
 // Carry pass of the chunked scan: per (b, d, n) an exclusive combine over the
 // K chunk (decay, end-state) pairs; writes every chunk's initial state into
 // ws_h in place (hin[k] = prod decay * h0 + ...).

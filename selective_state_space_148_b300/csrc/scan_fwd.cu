@@ -1,4 +1,7 @@
 // scan_fwd.cu -- instantiations and launch of the selective-scan kernel.
+#include <cstdlib>
+#include <cstring>
+
 #include "internal.h"
 
 namespace mamba {
@@ -69,8 +72,20 @@ static cudaError_t launch_t(int mode, bool vec, const ScanArgs &a, long long Bsz
     }
 }
 
+// The tensor-memory kernel serves N <= 16 (one 16-state group) on the 16-byte
+// aligned path; MAMBA_SCAN_KERNEL=smem selects the shared-memory kernel instead
+// (for comparison, or where tensor memory cannot be used).
+static bool use_tmem_kernel() {
+    static const int choice = [] {
+        const char *v = std::getenv("MAMBA_SCAN_KERNEL");
+        return (v != nullptr && std::strcmp(v, "smem") == 0) ? 0 : 1;
+    }();
+    return choice != 0;
+}
+
 cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long long Bsz, int grid_chunks,
                         cudaStream_t st) {
+    if (vec && a.N > 8 && a.N <= 16 && use_tmem_kernel()) return launch_scan_tm(dtype, mode, a, Bsz, grid_chunks, st);
     return dtype == 1 ? launch_t<bf16_t>(mode, vec, a, Bsz, grid_chunks, st)
                       : launch_t<float>(mode, vec, a, Bsz, grid_chunks, st);
 }
