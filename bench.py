@@ -70,41 +70,67 @@ def step_bytes(Bsz, Dch, N, io):
 
 # ----------------------------------------------------------------------------- clocks during the timed region
 
+class _Nvml:
+    """Minimal ctypes binding of libnvidia-ml (SM clock, max clock, clock-event reasons)."""
+    CLOCK_SM = 1
+
+    def __init__(self, pci_bus_id):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(self.h)) != 0:
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h)) != 0:
+                raise RuntimeError("no NVML device handle")
+        self._reasons = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+    def sm_clock(self):
+        v = self.ct.c_uint()
+        return v.value if self.lib.nvmlDeviceGetClockInfo(self.h, self.CLOCK_SM, self.ct.byref(v)) == 0 else None
+
+    def max_sm_clock(self):
+        v = self.ct.c_uint()
+        return v.value if self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.CLOCK_SM, self.ct.byref(v)) == 0 else None
+
+    def reasons(self):
+        v = self.ct.c_ulonglong()
+        return v.value if self._reasons(self.h, self.ct.byref(v)) == 0 else 0
+
+
 class ClockSampler:
-    """Polls NVML (SM clock, throttle reasons) in a thread while the timed region runs."""
+    """Samples the SM clock and clock-event (throttle) reasons while the timed region runs."""
 
     REASONS = {
         0x0000000000000008: "hw_slowdown", 0x0000000000000020: "sw_thermal_slowdown",
         0x0000000000000040: "hw_thermal_slowdown", 0x0000000000000004: "sw_power_cap",
-        0x0000000000000080: "hw_power_brake_slowdown", 0x0000000000000001: "gpu_idle",
-        0x0000000000000002: "applications_clocks_setting",
+        0x0000000000000080: "hw_power_brake_slowdown", 0x0000000000000002: "applications_clocks_setting",
     }
 
-    def __init__(self, device_index):
-        self.samples, self.reasons, self.max_mhz = [], set(), None
+    def __init__(self, pci_bus_id):
+        self.samples, self.reasons, self.max_mhz, self.source = [], set(), None, None
         self._stop = threading.Event()
         self._t = None
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self.nvml = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-        except Exception:
+            self.nvml = _Nvml(pci_bus_id)
+            self.max_mhz = self.nvml.max_sm_clock()
+            self.source = "nvml"
+        except Exception as e:  # noqa: BLE001
             self.nvml = None
+            self.error = str(e)
 
     def _run(self):
-        p = self.nvml
         while not self._stop.is_set():
-            try:
-                self.samples.append(p.nvmlDeviceGetClockInfo(self.h, p.NVML_CLOCK_SM))
-                r = p.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                for bit, name in self.REASONS.items():
-                    if r & bit and name != "gpu_idle":
-                        self.reasons.add(name)
-            except Exception:
-                break
-            time.sleep(0.002)
+            c = self.nvml.sm_clock()
+            if c is not None:
+                self.samples.append(c)
+            r = self.nvml.reasons()
+            for bit, name in self.REASONS.items():
+                if r & bit:
+                    self.reasons.add(name)
+            time.sleep(0.001)
 
     def __enter__(self):
         if self.nvml is not None:
@@ -118,10 +144,16 @@ class ClockSampler:
             self._t.join()
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons), "samples": 0}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
+               "reasons": sorted(self.reasons), "samples": len(self.samples), "source": self.source}
+        if self.nvml is None:
+            out["error"] = getattr(self, "error", "unavailable")
+        return out
+
+
+def pci_bus_id(torch):
+    p = torch.cuda.get_device_properties(torch.cuda.current_device())
+    return f"{getattr(p, 'pci_domain_id', 0):08x}:{getattr(p, 'pci_bus_id', 0):02x}:{getattr(p, 'pci_device_id', 0):02x}.0"
 
 
 # ----------------------------------------------------------------------------- MUFU peak
@@ -320,7 +352,7 @@ def bench_scan(args, m, torch):
         step(i)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as cs:
+    with ClockSampler(pci_bus_id(torch)) as cs:
         torch.cuda.synchronize()
         ev0.record(stream)
         for i in range(args.steps):
@@ -422,7 +454,7 @@ def bench_decode(args, m, torch):
         step(i)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(torch.cuda.current_device()) as cs:
+    with ClockSampler(pci_bus_id(torch)) as cs:
         ev0.record(stream)
         for i in range(args.steps):
             step(i)

@@ -95,6 +95,29 @@ __device__ __forceinline__ float2 gate2(float2 y, float2 z) {
     return f2(y.x * silu_f(z.x), y.y * silu_f(z.y));
 }
 
+// SiLU of a pair: FAST (bf16 storage) as (z / 2) (1 + tanh(z / 2)), one MUFU op
+// per element; otherwise the accurate scalar form above.
+template <bool FAST>
+__device__ __forceinline__ float2 silu2(float2 z) {
+    if (FAST) {
+        const float2 hz = __fmul2_rn(z, f2(0.5f, 0.5f));
+        return __ffma2_rn(hz, f2(tanh_approx(hz.x), tanh_approx(hz.y)), hz);
+    }
+    return f2(z.x * rcp_approx(1.0f + ex2_approx(-z.x * kLog2e)), z.y * rcp_approx(1.0f + ex2_approx(-z.y * kLog2e)));
+}
+
+// global stores that happen only where pred holds, without a branch around them
+__device__ __forceinline__ void st_b32_if(void *p, uint32_t v, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.global.b32 [%0], %1;\n\t}\n" ::"l"(p), "r"(v),
+                 "r"((uint32_t)pred)
+                 : "memory");
+}
+__device__ __forceinline__ void st_f32x2_if(void *p, float2 v, bool pred) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %3, 0;\n\t@q st.global.v2.f32 [%0], {%1, %2};\n\t}\n" ::"l"(p),
+                 "f"(v.x), "f"(v.y), "r"((uint32_t)pred)
+                 : "memory");
+}
+
 // ---------------------------------------------------------------- storage types
 struct bf16_t {  // tag type: 16-bit brain float stored as its bit pattern
     uint16_t bits;

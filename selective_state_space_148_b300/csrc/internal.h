@@ -26,7 +26,9 @@ cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long l
                         cudaStream_t st);
 
 // Tensor-memory variant of the scan kernel (N <= 16, 16-byte aligned rows):
-// B/C reach the registers through TMEM instead of shared memory.
+// B/C reach the registers through TMEM instead of shared memory, inputs arrive
+// by TMA.  Returns cudaErrorNotSupported, launching nothing, when the problem
+// does not fit its TMA descriptors (the caller then uses the other kernel).
 cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &a, long long Bsz, int grid_chunks, cudaStream_t st);
 
 // Carry pass of the chunked scan: per (b, d, n) an exclusive combine over the

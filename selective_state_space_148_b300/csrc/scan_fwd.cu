@@ -85,7 +85,12 @@ static bool use_tmem_kernel() {
 
 cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long long Bsz, int grid_chunks,
                         cudaStream_t st) {
-    if (vec && a.N > 8 && a.N <= 16 && use_tmem_kernel()) return launch_scan_tm(dtype, mode, a, Bsz, grid_chunks, st);
+    // (its TMA boxes start on 32-step boundaries: chunks must be whole super-tiles;
+    // it declines, with cudaErrorNotSupported, problems its descriptors cannot express)
+    if (vec && a.N > 8 && a.N <= 16 && (a.nchunks == 1 || a.chunk_len % 32 == 0) && use_tmem_kernel()) {
+        const cudaError_t e = launch_scan_tm(dtype, mode, a, Bsz, grid_chunks, st);
+        if (e != cudaErrorNotSupported) return e;
+    }
     return dtype == 1 ? launch_t<bf16_t>(mode, vec, a, Bsz, grid_chunks, st)
                       : launch_t<float>(mode, vec, a, Bsz, grid_chunks, st);
 }

@@ -1,5 +1,8 @@
-// scan_tm.cu -- instantiations and launch of the tensor-memory scan kernel, and
-// the device error word it reports bounded-wait timeouts in.
+// scan_tm.cu -- instantiations and launch of the tensor-memory scan kernel
+// (TMA descriptors, launch geometry), and the device error word it reports
+// bounded-wait timeouts in.
+#include <cuda.h>
+
 #include "../../include/mamba_scan.h"
 #include "internal.h"
 
@@ -11,10 +14,52 @@ __device__ unsigned int g_device_error = 0;
 
 namespace mamba {
 
+namespace {
+
+constexpr int kNwg = 3;  // warpgroups per CTA: 96 channels, one CTA per SM
+
+// cuTensorMapEncodeTiled, reached through the runtime's driver entry point so
+// that the library does not link the driver library itself
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static const EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<EncodeTiledFn>(nullptr);
+        }
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// [outer][mid][inner] tensor, box of 32 x box_mid x 1 elements
+bool encode_3d(CUtensorMap *m, const void *ptr, bool bf16, long long inner, long long mid, long long outer,
+               unsigned box_mid, bool swizzle) {
+    const EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t es = bf16 ? 2 : 4;
+    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)outer};
+    const cuuint64_t strides[2] = {(cuuint64_t)inner * es, (cuuint64_t)inner * (cuuint64_t)mid * es};
+    const cuuint32_t box[3] = {32u, box_mid, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUtensorMapSwizzle sw =
+        !swizzle ? CU_TENSOR_MAP_SWIZZLE_NONE : (bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
+    return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(ptr),
+              dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <typename T, int MODE>
-static cudaError_t launch_tm_one(const ScanArgs &a, long long Bsz, int grid_chunks, cudaStream_t st) {
-    using Sh = TmShape<T, MODE>;
-    auto kern = scan_tm_kernel<T, MODE>;
+cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, long long Bsz, int grid_chunks, cudaStream_t st) {
+    using Sh = TmShape<T, MODE, kNwg>;
+    auto kern = scan_tm_kernel<T, MODE, kNwg>;
     static bool attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -25,16 +70,29 @@ static cudaError_t launch_tm_one(const ScanArgs &a, long long Bsz, int grid_chun
         if (dev >= 0 && dev < kMaxDevices) attr_set[dev] = true;
     }
     dim3 grid((unsigned)((a.Dch + Sh::CH - 1) / Sh::CH), (unsigned)Bsz, (unsigned)grid_chunks);
-    kern<<<grid, Sh::NTHR, Sh::SMEM_BYTES, st>>>(a);
+    kern<<<grid, Sh::NTHR, Sh::SMEM_BYTES, st>>>(a, maps);
     return cudaGetLastError();
 }
 
+}  // namespace
+
 cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &a, long long Bsz, int grid_chunks, cudaStream_t st) {
-    if (dtype == 1)
-        return mode == MODE_FULL ? launch_tm_one<bf16_t, MODE_FULL>(a, Bsz, grid_chunks, st)
-                                 : launch_tm_one<bf16_t, MODE_STATES>(a, Bsz, grid_chunks, st);
-    return mode == MODE_FULL ? launch_tm_one<float, MODE_FULL>(a, Bsz, grid_chunks, st)
-                             : launch_tm_one<float, MODE_STATES>(a, Bsz, grid_chunks, st);
+    // TMA coordinates are 32-bit: the time axis and the channel axis must fit
+    if (a.L >= (1LL << 31) - 64 || a.Dch >= (1LL << 31) - 128 || Bsz >= (1LL << 31)) return cudaErrorNotSupported;
+    const bool bf16 = dtype == 1;
+    constexpr int CH = 32 * kNwg;
+    TmMaps maps;
+    bool ok = encode_3d(&maps.u, a.u, bf16, a.L, a.Dch, Bsz, CH, true) &&
+              encode_3d(&maps.delta, a.delta, bf16, a.L, a.Dch, Bsz, CH, true) &&
+              encode_3d(&maps.z, a.z != nullptr ? a.z : a.u, bf16, a.L, a.Dch, Bsz, CH, true) &&
+              encode_3d(&maps.B, a.Bm, bf16, a.L, a.N, Bsz, 16, false) &&
+              encode_3d(&maps.C, a.Cm, bf16, a.L, a.N, Bsz, 16, false);
+    if (!ok) return cudaErrorNotSupported;
+    if (bf16)
+        return mode == MODE_FULL ? launch_tm_one<bf16_t, MODE_FULL>(a, maps, Bsz, grid_chunks, st)
+                                 : launch_tm_one<bf16_t, MODE_STATES>(a, maps, Bsz, grid_chunks, st);
+    return mode == MODE_FULL ? launch_tm_one<float, MODE_FULL>(a, maps, Bsz, grid_chunks, st)
+                             : launch_tm_one<float, MODE_STATES>(a, maps, Bsz, grid_chunks, st);
 }
 
 }  // namespace mamba

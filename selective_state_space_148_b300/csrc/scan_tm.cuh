@@ -1,7 +1,8 @@
 // scan_tm.cuh -- selective scan for N <= 16 with B/C broadcast through tensor memory.
 //
 // Same arithmetic as scan_kernel (fsdata.site explainer §3.2 selective_step;
-// freeguideonline tutorial §4.2, §4.3, §5.2), different operand delivery.
+// freeguideonline tutorial §4.2, §4.3, §5.2), different operand delivery and
+// schedule.
 //
 // Why: on B300 the MUFU pipe issues 32 ex2 per SM per clock, while a 16-byte
 // shared-memory load costs four L1 wavefronts (one per quarter warp) even when
@@ -19,19 +20,37 @@
 // values along K (bf16 storage: one bf16 each, exact; fp32 storage: each value
 // split into three bf16 parts hi+mid+lo whose fp32 sum reproduces it, K rows
 // 3s..3s+2).  D lands in TMEM as fp32; thread m reads its lane with
-// tcgen05.ld.  One MMA (M=128, N=64, K=16) covers 8 steps.  Pairing the columns
-// by time lets the f32x2 instructions take (Delta_t, Delta_t+1) against a
-// duplicated (A_n, A_n) and (Delta u) pairs against (B_n(t), B_n(t+1)) without
-// register moves; the h recurrence stays scalar.
+// tcgen05.ld.  Pairing the columns by time lets the f32x2 instructions take
+// (Delta_t, Delta_t+1) against a duplicated (A_n, A_n) and (Delta u) pairs
+// against (B_n(t), B_n(t+1)) without register moves; the h recurrence stays
+// scalar.
 //
-// Mapping: 128 threads = 128 TMEM lanes; thread m owns channel m/4 (32
-// channels per CTA) and states 4*(m%4)..+3.  Time advances in super-tiles of
-// 32 steps (u/Delta_raw/z loads, one softplus per (b,d,t) shared through
-// shared memory, the y output) made of 4 MMA tiles of 8 steps; TMEM holds two
-// tiles (double buffer, 128 columns), the X operand two super-tiles.  Every
-// mbarrier wait is bounded; a timeout is agreed block-wide, recorded in the
-// device error word, and the CTA frees its TMEM and returns.
+// B and C do not depend on the channel, so every warpgroup of a CTA reads the
+// same TMEM columns: a CTA of NWG warpgroups (32 channels each, 4 lanes per
+// channel, lane m%4 owning states 4(m%4)..+3) takes the whole of TMEM (512
+// columns, one CTA per SM) as two buffers of one 32-step super-tile each.  Per
+// super-tile the CTA does, once: one MMA (M=128, N=256, K=16), five tiled TMA
+// loads (u, Delta_raw, z boxes of 32 steps x 32 NWG channels, B and C boxes of
+// 32 steps x 16 states; out-of-range rows and steps read as zero), one X build
+// and one CTA barrier.  The input ring has 3 stages, loaded two super-tiles
+// ahead; u/Delta_raw/z use the TMA's 16-byte-chunk swizzle so that the 8
+// channels of a warp hit distinct banks.
+//
+// Per 8-step sub-tile i each lane loads its 64 TMEM columns, then in one
+// branch-free block computes Delta = softplus(.), Delta*u, D*u and SiLU(z) for
+// its step pair of sub-tile i+1 (Delta, Delta*u go to shared memory for the
+// channel's 4 lanes; D*u, SiLU(z) stay in registers), finishes y for its pair
+// of sub-tile i-1 (sum of the 4 lanes' C.h partials, + D*u, * SiLU(z),
+// predicated store) and runs the recurrence over sub-tile i's 8 steps.
+//
+// Every mbarrier wait is bounded; a timeout sets a shared abort flag that
+// every later wait honours and that stops further loads, is recorded in the
+// device error word, and the CTA still walks its loop (no further MMAs or
+// TMEM loads), waits (bounded) for its issued MMAs and loads, frees its TMEM
+// and returns.
 #pragma once
+
+#include <cuda.h>
 
 #include "scan_kernels.cuh"
 #include "tcgen05.cuh"
@@ -42,63 +61,74 @@ namespace mamba {
 // header, scan_tm.cu, before the include).  Bit 0: an mbarrier wait of the
 // tensor-memory scan timed out.
 
-template <typename T, int MODE>
-struct TmShape {
-    static constexpr int NTHR = 128, CH = 32, S = 4, NS = 4;
-    static constexpr int TT = 32;              // super-tile (steps)
-    static constexpr int TB = 8;               // MMA tile (steps)
-    static constexpr int NTILE = TT / TB;      // MMA tiles per super-tile
-    static constexpr int COLS = 8 * TB;        // TMEM columns per tile (B[4], C[4] per step)
-    static constexpr int TMEM_COLS = 2 * COLS; // double buffered
-    static constexpr int SEG = TT / S;         // steps per lane segment (Delta, u, z, y)
-    static constexpr int PER16 = 16 / (int)sizeof(T);
-    static constexpr int W = SEG / PER16;      // 16-byte vectors per lane segment
-    static constexpr bool SPLIT = sizeof(T) == 4;
-    static constexpr int CPR = TT * (int)sizeof(T) / 16;  // 16-byte chunks per B/C row and super-tile
-    static constexpr int NCHUNK = 2 * 16 * CPR;            // B and C, 16 rows
-    static constexpr int RAW_PER_THR = NCHUNK / NTHR;      // 1 (bf16) or 2 (fp32)
-    static constexpr int A_BYTES = 128 * 16 * 2;
-    static constexpr int X_STEP = 256;         // bytes per step: 8 columns x 16 K bf16 (one 8-row group)
-    static constexpr int X_BYTES = TT * X_STEP;
-    static constexpr int RAW_BYTES = 2 * 16 * TT * (int)sizeof(T);
-    static constexpr int DU_STRIDE = TT * 2 + 4;
-    static constexpr int P_STRIDE = TT + 4;
-    static constexpr int OFF_X = A_BYTES;
-    static constexpr int OFF_RAW = OFF_X + 2 * X_BYTES;
-    static constexpr int OFF_DU = OFF_RAW + RAW_BYTES;
-    static constexpr int OFF_P = OFF_DU + CH * DU_STRIDE * 4;
-    static constexpr int OFF_BAR = OFF_P + (MODE == MODE_FULL ? CH * S * P_STRIDE * 4 : 0);
-    static constexpr int USED = OFF_BAR + 32;
-    // at most four CTAs per SM: four x 128 TMEM columns is the whole of TMEM, so
-    // the dynamic shared memory is padded until a fifth CTA cannot be resident
-    static constexpr int SMEM_BYTES = USED > 47 * 1024 ? USED : 47 * 1024;
-    static_assert(NCHUNK % NTHR == 0, "B/C staging must split evenly over the CTA");
-    static_assert(W >= 1, "lane segment must be whole 16-byte vectors");
+// TMA descriptors of one call: u, Delta_raw, z as [Bsz][Dch][L] with boxes of
+// 32 steps x CH channels (swizzled); B, C as [Bsz][N][L] with boxes of 32
+// steps x 16 states (plain).
+struct TmMaps {
+    CUtensorMap u, delta, z, B, C;
 };
 
-template <typename T, int MODE>
-__global__ void __launch_bounds__(128, 3)
-scan_tm_kernel(const ScanArgs a) {
-    using Sh = TmShape<T, MODE>;
-    using IO = Io<T>;
+template <typename T, int MODE, int NWG>
+struct TmShape {
+    static constexpr int NTHR = 128 * NWG, CH = 32 * NWG, S = 4;
+    static constexpr int TT = 32;                  // steps per super-tile
+    static constexpr int TB = 8;                   // steps per sub-tile
+    static constexpr int NSUB = TT / TB;
+    static constexpr int COLS = 8 * TT;            // TMEM columns per super-tile (B[4], C[4] per step)
+    static constexpr int TMEM_COLS = 2 * COLS;     // 512: all of TMEM, one CTA per SM
+    static constexpr int NST = 3;                  // input stages
+    static constexpr bool SPLIT = sizeof(T) == 4;
+    static constexpr int ROW = TT * (int)sizeof(T);  // bytes of one row of a box
+    static constexpr int SWZ = ROW / 16;             // 16-byte chunks per swizzle span (64 B or 128 B)
+    static constexpr int IO_TILE = CH * ROW;         // one of u, Delta_raw, z
+    static constexpr int BC_TILE = 16 * ROW;         // one of B, C
+    static constexpr int STAGE_BYTES = 3 * IO_TILE + 2 * BC_TILE;
+    static constexpr int A_BYTES = 128 * 16 * 2;
+    static constexpr int X_BYTES = COLS * 16 * 2;
+    static constexpr int DU_BYTES = CH * S * 16;           // per sub-tile: (Delta, Delta', du, du') per lane
+    static constexpr int P_STRIDE = TB + 4;                // floats per (channel, lane) row of partials
+    static constexpr int P_BYTES = CH * S * P_STRIDE * 4;  // per sub-tile
+    static constexpr int OFF_ST = 0;
+    static constexpr int OFF_A = OFF_ST + NST * STAGE_BYTES;
+    static constexpr int OFF_X = OFF_A + A_BYTES;
+    static constexpr int OFF_DU = OFF_X + 2 * X_BYTES;
+    static constexpr int OFF_P = OFF_DU + 2 * DU_BYTES;
+    static constexpr int OFF_BAR = OFF_P + (MODE == MODE_FULL ? 2 * P_BYTES : 0);
+    static constexpr int SMEM_BYTES = OFF_BAR + 128 + 1024;  // + room to align the base to 1024 bytes
+    static_assert(IO_TILE % 1024 == 0 && BC_TILE % 1024 == 0, "swizzled boxes need 1024-byte aligned tiles");
+    static_assert(SWZ == 4 || SWZ == 8, "rows of 64 or 128 bytes");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
+};
+
+template <typename T, int MODE, int NWG>
+__global__ void __launch_bounds__(128 * NWG, 1)
+scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
+    using Sh = TmShape<T, MODE, NWG>;
     constexpr bool FAST = sizeof(T) == 2;
-    constexpr int S = Sh::S, SEG = Sh::SEG, PER16 = Sh::PER16, W = Sh::W, TT = Sh::TT, TB = Sh::TB;
-    constexpr int NTILE = Sh::NTILE, COLS = Sh::COLS, CPR = Sh::CPR;
+    constexpr int S = Sh::S, TT = Sh::TT, TB = Sh::TB, NSUB = Sh::NSUB, COLS = Sh::COLS, CH = Sh::CH;
+    constexpr int NST = Sh::NST, NTHR = Sh::NTHR;
     constexpr uint32_t kWaitPolls = 1u << 24;
     constexpr uint32_t kIdesc = tc::umma_idesc_bf16_f32(128, COLS);
+    using Word = typename std::conditional<Sh::SPLIT, float2, uint32_t>::type;  // one step pair
 
-    extern __shared__ __align__(1024) unsigned char smem[];
-    uint16_t *const sA = reinterpret_cast<uint16_t *>(smem);
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *const smem = smem_raw + ((1024u - (tc::smem_addr(smem_raw) & 1023u)) & 1023u);
+    unsigned char *const sSt = smem + Sh::OFF_ST;
+    uint16_t *const sA = reinterpret_cast<uint16_t *>(smem + Sh::OFF_A);
     unsigned char *const sX = smem + Sh::OFF_X;
-    unsigned char *const sRaw = smem + Sh::OFF_RAW;
-    float *const sDU = reinterpret_cast<float *>(smem + Sh::OFF_DU);
-    float *const sP = reinterpret_cast<float *>(smem + Sh::OFF_P);
-    uint64_t *const mbar = reinterpret_cast<uint64_t *>(smem + Sh::OFF_BAR);
-    uint32_t *const taddr_s = reinterpret_cast<uint32_t *>(smem + Sh::OFF_BAR + 16);
+    float4 *const sDU = reinterpret_cast<float4 *>(smem + Sh::OFF_DU);  // [2][CH][S]
+    float *const sP = reinterpret_cast<float *>(smem + Sh::OFF_P);      // [2][CH][S][P_STRIDE]
+    uint64_t *const full = reinterpret_cast<uint64_t *>(smem + Sh::OFF_BAR);  // [2] MMA of a super-tile done
+    uint64_t *const xready = full + 2;                                        // X built by every warp
+    uint64_t *const done = full + 3;                                          // abort path: all MMAs done
+    uint64_t *const io = full + 4;                                            // [NST] stage loads landed
+    uint32_t *const taddr_s = reinterpret_cast<uint32_t *>(smem + Sh::OFF_BAR + 64);
+    volatile int *const abort_flag = reinterpret_cast<volatile int *>(smem + Sh::OFF_BAR + 68);
 
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int s = tid & 3, c = tid >> 2;
-    const long long d = (long long)blockIdx.x * Sh::CH + c;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int s = tid & 3, c = tid >> 2;  // channel within the CTA, state slice
+    const long long d0 = (long long)blockIdx.x * CH;
+    const long long d = d0 + c;
     const bool valid = d < a.Dch;
     const long long b = blockIdx.y;
     const int kch = blockIdx.z;
@@ -106,11 +136,10 @@ scan_tm_kernel(const ScanArgs a) {
     const long long t_begin = (long long)kch * a.chunk_len;
     const long long t_end = min(L, t_begin + a.chunk_len);
     const int nsup = (int)((t_end - t_begin + TT - 1) / TT);
-    const int ntile = nsup * NTILE;
     const long long dd = valid ? d : 0;
     const long long row = (b * a.Dch + dd) * L;
-    const long long bc_row0 = b * N * L;
     const bool has_z = a.z != nullptr;
+    const bool load_z = MODE == MODE_FULL && has_z;
 
     // ---------------------------------------------------------------- one-time set-up
     if (warp == 0) {
@@ -118,16 +147,20 @@ scan_tm_kernel(const ScanArgs a) {
         tc::tmem_relinquish();
     }
     // selector: element (m, k) of the 128 x 16 K-major operand
-    for (int i = tid; i < 128 * 16; i += Sh::NTHR) {
+    for (int i = tid; i < 128 * 16; i += NTHR) {
         const int m = i >> 4, kk = i & 15;
         const bool one = Sh::SPLIT ? (kk < 12 && kk / 3 == (m & 3)) : (kk == (m & 3));
         sA[((m >> 3) * 256 + (kk >> 3) * 128 + (m & 7) * 16 + (kk & 7) * 2) >> 1] = one ? 0x3F80u : 0u;
     }
-    for (int i = tid; i < 2 * Sh::X_BYTES / 16; i += Sh::NTHR)
+    for (int i = tid; i < 2 * Sh::X_BYTES / 16; i += NTHR)
         reinterpret_cast<uint4 *>(sX)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) {
-        tc::mbar_init(&mbar[0], 1);
-        tc::mbar_init(&mbar[1], 1);
+        tc::mbar_init(&full[0], 1);
+        tc::mbar_init(&full[1], 1);
+        tc::mbar_init(xready, NTHR / 32);
+        tc::mbar_init(done, 1);
+        for (int k = 0; k < NST; ++k) tc::mbar_init(&io[k], 1);
+        *abort_flag = 0;
         tc::fence_mbar_init();
     }
 
@@ -145,43 +178,39 @@ scan_tm_kernel(const ScanArgs a) {
     }
     const float Dd = (a.D != nullptr && valid) ? a.D[dd] : 0.f;
     const float bias = (a.bias != nullptr && valid) ? a.bias[dd] : 0.f;
+    const float2 bias2 = f2(bias, bias);
+    const float2 D2 = f2(Dd, Dd);
 
-    // ---- B/C staging: raw rows of one super-tile (chunk q -> tensor, state row, 16-byte chunk)
-    uint4 rraw[Sh::RAW_PER_THR];
-    auto raw_load = [&](int sup) {
-        const long long t0 = t_begin + (long long)sup * TT;
-#pragma unroll
-        for (int r = 0; r < Sh::RAW_PER_THR; ++r) {
-            const int q = tid + r * Sh::NTHR;
-            const int chunk = q % CPR, n = (q / CPR) & 15, which = q / (16 * CPR);
-            const void *base = which ? a.Cm : a.Bm;
-            const long long tt = t0 + (long long)chunk * PER16;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (n < N && tt < t_end) {
-                const long long off = bc_row0 + n * L + tt;
-                if (tt + PER16 <= t_end) {
-                    v = ldg16(reinterpret_cast<const T *>(base) + off);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < PER16; ++i)
-                        if (tt + i < t_end) IO::set(v, i, IO::load(base, off + i));
-                }
-            }
-            rraw[r] = v;
+    // bounded wait that gives up at once when another warp has already given up
+    auto wait_or_abort = [&](uint64_t *bar, uint32_t parity) -> bool {
+        for (uint32_t it = 0;; ++it) {
+            if (tc::mbar_test_wait(bar, parity)) return true;
+            if (*abort_flag != 0 || it >= kWaitPolls) return false;
         }
     };
-    auto raw_store = [&]() {
-#pragma unroll
-        for (int r = 0; r < Sh::RAW_PER_THR; ++r)
-            reinterpret_cast<uint4 *>(sRaw)[tid + r * Sh::NTHR] = rraw[r];
+
+    // ---- inputs of super-tile sn -> stage sn % NST (thread 0).  The time
+    // coordinate is a multiple of 32 steps, so x * element size is a multiple
+    // of 16 bytes.
+    auto stage_of = [&](int k) { return sSt + k * Sh::STAGE_BYTES; };
+    auto load_stage = [&](int sn) {
+        unsigned char *st = stage_of(sn % NST);
+        uint64_t *bar = &io[sn % NST];
+        const int x = (int)(t_begin + (long long)sn * TT);
+        tc::mbar_arrive_expect_tx(bar, (uint32_t)((load_z ? 3 : 2) * Sh::IO_TILE + 2 * Sh::BC_TILE));
+        tc::tma_load_3d(st, &maps.u, x, (int)d0, (int)b, bar);
+        tc::tma_load_3d(st + Sh::IO_TILE, &maps.delta, x, (int)d0, (int)b, bar);
+        if (load_z) tc::tma_load_3d(st + 2 * Sh::IO_TILE, &maps.z, x, (int)d0, (int)b, bar);
+        tc::tma_load_3d(st + 3 * Sh::IO_TILE, &maps.B, x, 0, (int)b, bar);
+        tc::tma_load_3d(st + 3 * Sh::IO_TILE + Sh::BC_TILE, &maps.C, x, 0, (int)b, bar);
     };
-    // X for one super-tile from sRaw: column n = 16 * pair + j (see the column order above)
-    auto x_build = [&](int xb) {
-        const T *raw = reinterpret_cast<const T *>(sRaw);  // [which][16][TT]
+    int last_loaded = -1;  // thread 0: latest super-tile whose loads were issued
+
+    // X of one super-tile from its stage: column n = 16 * pair + j (column order above)
+    auto x_build = [&](int xb, const unsigned char *st) {
+        const T *raw = reinterpret_cast<const T *>(st + 3 * Sh::IO_TILE);  // [which][16][TT]
         unsigned char *xbase = sX + xb * Sh::X_BYTES;
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-            const int n = tid + r * Sh::NTHR;  // 256 columns
+        for (int n = tid; n < COLS; n += NTHR) {
             const int j = n & 15;
             const int t = 2 * (n >> 4) + (j & 1);
             const int which = j >> 3, col = (j & 7) >> 1;
@@ -217,216 +246,183 @@ scan_tm_kernel(const ScanArgs a) {
         }
     };
 
-    // ---- per-lane segment of u, Delta_raw, z
-    uint4 ru[W], rd[W], rz[W];
-    auto seg_load = [&](int sup, uint4 (&xu)[W], uint4 (&xd)[W], uint4 (&xz)[W]) {
-        const long long t0 = t_begin + (long long)sup * TT + (long long)s * SEG;
-        const T *pu = reinterpret_cast<const T *>(a.u) + row + t0;
-        const T *pd = reinterpret_cast<const T *>(a.delta) + row + t0;
-        const T *pz = reinterpret_cast<const T *>(a.z) + row + t0;
-        if (valid && t0 + SEG <= t_end) {
-#pragma unroll
-            for (int w = 0; w < W; ++w) {
-                xu[w] = ldg16(pu + w * PER16);
-                xd[w] = ldg16(pd + w * PER16);
-                xz[w] = has_z ? ldg16(pz + w * PER16) : make_uint4(0u, 0u, 0u, 0u);
-            }
-        } else {
-#pragma unroll
-            for (int w = 0; w < W; ++w) {
-                uint4 vu = make_uint4(0u, 0u, 0u, 0u), vd = vu, vz = vu;
-#pragma unroll
-                for (int i = 0; i < PER16; ++i) {
-                    const long long t = t0 + w * PER16 + i;
-                    if (valid && t < t_end) {
-                        IO::set(vu, i, IO::load(a.u, row + t));
-                        IO::set(vd, i, IO::load(a.delta, row + t));
-                        if (has_z) IO::set(vz, i, IO::load(a.z, row + t));
-                    }
-                }
-                xu[w] = vu;
-                xd[w] = vd;
-                xz[w] = vz;
-            }
+    // ---- per-lane step pair (t0, t0 + 1) of sub-tile i, t0 = t_begin + 8 i + 2 s.
+    // t_end is even on the vectorised path, so a pair lies wholly inside or
+    // wholly outside [t_begin, t_end).
+    auto pair_t0 = [&](int i) { return t_begin + (long long)i * TB + 2 * s; };
+    auto unpack = [](Word w) -> float2 {
+        if constexpr (Sh::SPLIT) return w;
+        else return f2(bf16_lo(w), bf16_hi(w));
+    };
+    // this lane's pair of sub-tile q of a stage; the box rows are swizzled:
+    // 16-byte chunk k of row r sits at chunk k ^ (r mod SWZ) ... of the
+    // 1024-byte aligned pattern, i.e. byte offset o -> o ^ (((o >> 7) % SWZ) << 4)
+    auto stage_word = [&](const unsigned char *st, int tensor, int q) -> Word {
+        const int o = c * Sh::ROW + (q * TB + 2 * s) * (int)sizeof(T);
+        const int osw = o ^ (((o >> 7) & (Sh::SWZ - 1)) << 4);
+        return *reinterpret_cast<const Word *>(st + tensor * Sh::IO_TILE + osw);
+    };
+    // Delta, Delta * u -> sDU[i & 1][c][s] (read by the channel's 4 lanes);
+    // D * u and SiLU(z) stay in this lane's registers until y of the pair is formed
+    float sdt_acc = 0.f;  // MODE_STATES: this lane's share of sum(Delta) over the chunk
+    auto side_pair = [&](const unsigned char *st, int q, int i, float2 &Du, float2 &g) {
+        const bool in = valid && pair_t0(i) < t_end;
+        const float2 u = unpack(stage_word(st, 0, q));
+        const float2 raw = __fadd2_rn(unpack(stage_word(st, 1, q)), bias2);
+        float2 dl = a.softplus ? softplus2<FAST>(raw) : raw;
+        float2 du = __fmul2_rn(dl, u);
+        if (!in) dl = du = f2(0.f, 0.f);
+        sDU[((i & 1) * CH + c) * S + s] = make_float4(dl.x, dl.y, du.x, du.y);
+        if (MODE == MODE_STATES) sdt_acc += dl.x + dl.y;
+        if (MODE == MODE_FULL) {
+            Du = __fmul2_rn(D2, u);
+            g = has_z ? silu2<FAST>(unpack(stage_word(st, 2, q))) : f2(1.f, 1.f);
         }
     };
+    // y of this lane's step pair of sub-tile i from the channel's 4 partial sums
+    auto output_pair = [&](int i, float2 Du, float2 g) {
+        if (MODE != MODE_FULL) return;
+        const float *pp = sP + ((i & 1) * CH + c) * S * Sh::P_STRIDE + 2 * s;
+        float2 ys = *reinterpret_cast<const float2 *>(pp);
+#pragma unroll
+        for (int r = 1; r < S; ++r) ys = __fadd2_rn(ys, *reinterpret_cast<const float2 *>(pp + r * Sh::P_STRIDE));
+        const float2 yy = __fmul2_rn(__fadd2_rn(ys, Du), g);
+        const long long t0 = pair_t0(i);
+        const bool st = valid && t0 >= t_begin && t0 < t_end;
+        if constexpr (Sh::SPLIT)
+            st_f32x2_if(reinterpret_cast<float *>(a.y) + row + t0, yy, st);
+        else
+            st_b32_if(reinterpret_cast<uint16_t *>(a.y) + row + t0, pack_bf16x2(yy.x, yy.y), st);
+    };
 
-    // ---- prologue: X of super-tile 0 built, the first two MMA tiles issued
-    raw_load(0);
-    seg_load(0, ru, rd, rz);
-    raw_store();
+    const uint64_t descA = tc::umma_desc(tc::smem_addr(sA), 128, 256);
+    auto issue_mma = [&](int sn) {  // thread 0: MMA of super-tile sn -> TMEM buffer sn & 1, completion on full[sn & 1]
+        const uint32_t xaddr = tc::smem_addr(sX + (sn & 1) * Sh::X_BYTES);
+        tc::fence_after_sync();
+        tc::umma_bf16(*taddr_s + (sn & 1) * COLS, descA, tc::umma_desc(xaddr, 128, 256), kIdesc, 0u);
+        tc::umma_commit(&full[sn & 1]);
+    };
+
+    // ---- prologue: loads of super-tiles 0 and 1, X and MMA of super-tile 0, Delta of sub-tile 0
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem_base = *taddr_s;
-    const uint32_t tmem_lane = tmem_base + (static_cast<uint32_t>(warp * 32) << 16);
-    x_build(0);
-    if (nsup > 1) raw_load(1);
+    const uint32_t tmem_lane = *taddr_s + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    if (tid == 0) {
+        load_stage(0);
+        last_loaded = 0;
+        if (nsup > 1) {
+            load_stage(1);
+            last_loaded = 1;
+        }
+    }
+    if (!wait_or_abort(&io[0], 0)) *abort_flag = 1;
+    x_build(0, stage_of(0));
     tc::fence_proxy_async();
     __syncthreads();
-    const uint64_t descA = tc::umma_desc(tc::smem_addr(sA), 128, 256);
-    auto issue = [&](int i) {  // MMA tile i -> TMEM buffer i & 1, completion on mbar[i & 1]
-        const uint32_t xaddr = tc::smem_addr(sX + ((i / NTILE) & 1) * Sh::X_BYTES + (i % NTILE) * TB * Sh::X_STEP);
-        tc::umma_bf16(tmem_base + (i & 1) * COLS, descA, tc::umma_desc(xaddr, 128, 256), kIdesc, 0u);
-        tc::umma_commit(&mbar[i & 1]);
-    };
-    if (tid == 0) {
-        tc::fence_after_sync();
-        issue(0);
-        if (ntile > 1) issue(1);
+    int mma_issued = 0;  // thread 0
+    if (tid == 0 && *abort_flag == 0) {
+        issue_mma(0);
+        mma_issued = 1;
     }
+    // (D u, SiLU z) of the step pairs whose y is still open, by sub-tile parity
+    float2 Du_r[2], g_r[2];
+    side_pair(stage_of(0), 0, 0, Du_r[0], g_r[0]);
+    __syncwarp();
 
-    float sdt_acc = 0.f;
-    float *const du_c = sDU + c * Sh::DU_STRIDE;
-    const float2 bias2 = f2(bias, bias);
-    const float2 D2 = f2(Dd, Dd);
-    bool failed = false;
-
-    for (int sup = 0; sup < nsup && !failed; ++sup) {
-        const bool has_next = sup + 1 < nsup;
-        // X of the next super-tile (its raw rows were loaded one super-tile ago)
-        if (has_next) {
-            raw_store();
-            __syncthreads();
-            x_build((sup + 1) & 1);
-            tc::fence_proxy_async();
-            if (sup + 2 < nsup) raw_load(sup + 2);
-        }
-        uint4 nu[W], nd[W], nz[W];
-        if (has_next) seg_load(sup + 1, nu, nd, nz);
-
-        // Delta and Delta*u for this lane's 8 steps, shared with the channel's other lanes
-        const long long tseg = t_begin + (long long)sup * TT + (long long)s * SEG;
-        const bool seg_full = valid && tseg + SEG <= t_end;
-#pragma unroll
-        for (int i = 0; i < SEG; i += 2) {
-            const float2 raw = __fadd2_rn(f2(IO::get(rd[i / PER16], i % PER16),
-                                             IO::get(rd[(i + 1) / PER16], (i + 1) % PER16)), bias2);
-            float2 dl = a.softplus ? softplus2<FAST>(raw) : raw;
-            if (!seg_full) {
-                if (!(valid && tseg + i < t_end)) dl.x = 0.f;
-                if (!(valid && tseg + i + 1 < t_end)) dl.y = 0.f;
-            }
-            const float2 du = __fmul2_rn(dl, f2(IO::get(ru[i / PER16], i % PER16),
-                                                IO::get(ru[(i + 1) / PER16], (i + 1) % PER16)));
-            *reinterpret_cast<float4 *>(du_c + (s * SEG + i) * 2) = make_float4(dl.x, dl.y, du.x, du.y);
-            if (MODE == MODE_STATES) sdt_acc += dl.x + dl.y;
-        }
-        __syncwarp();
-
-        float *const prow = sP + (c * S + s) * Sh::P_STRIDE;
-#pragma unroll
-        for (int q = 0; q < NTILE; ++q) {
-            const int i = sup * NTILE + q;
-            // warp-uniform outcome: tcgen05.ld below is .sync.aligned
-            const bool ok = __all_sync(0xffffffffu, tc::mbar_wait_bounded(&mbar[i & 1], (i >> 1) & 1, kWaitPolls));
-            tc::fence_after_sync();
-            float bc[64];
-            if (ok) {
-                float *b0 = bc, *b1 = bc + 32;
-                tc::tmem_ld32_wait(tmem_lane + (i & 1) * COLS, *reinterpret_cast<float(*)[32]>(b0));
-                tc::tmem_ld32_wait(tmem_lane + (i & 1) * COLS + 32, *reinterpret_cast<float(*)[32]>(b1));
-            }
+    int k_cur = 0;  // stage of super-tile sup
+    for (int sup = 0; sup < nsup; ++sup) {
+        const int k_nxt = k_cur == NST - 1 ? 0 : k_cur + 1;
+        if (sup + 1 < nsup) {
+            // Every warp has finished super-tile sup - 1: TMEM buffer (sup + 1) & 1
+            // and X buffer (sup + 1) & 1 are free (their MMA was waited for), and
+            // so is the stage of sup - 1, which the loads of sup + 2 reuse.
             tc::fence_before_sync();
-            if (__syncthreads_or(!ok)) {
-                failed = true;
-                break;
+            __syncthreads();
+            tc::fence_after_sync();
+            if (tid == 0 && sup + 2 < nsup && *abort_flag == 0) {
+                load_stage(sup + 2);
+                last_loaded = sup + 2;
             }
-            if (tid == 0 && i + 2 < ntile) {
-                tc::fence_after_sync();
-                issue(i + 2);
+            if (!wait_or_abort(&io[k_nxt], ((sup + 1) / NST) & 1)) *abort_flag = 1;
+            x_build((sup + 1) & 1, stage_of(k_nxt));
+            tc::fence_proxy_async();
+            __syncwarp();
+            tc::mbar_arrive_if(xready, lane == 0);
+            if (tid == 0) {
+                if (wait_or_abort(xready, sup & 1) && *abort_flag == 0) {
+                    issue_mma(sup + 1);
+                    mma_issued = sup + 2;
+                } else {
+                    *abort_flag = 1;
+                }
             }
-            // all of the tile's shared-memory inputs first: (Delta, Delta', du, du') per step pair
-            float4 dd[TB / 2];
+        }
+        // this super-tile's B/C are in TMEM buffer sup & 1
+        const bool ok = __all_sync(0xffffffffu, wait_or_abort(&full[sup & 1], (sup >> 1) & 1));
+        tc::fence_after_sync();
+        if (!ok) *abort_flag = 1;
+        const unsigned char *st_cur = stage_of(k_cur);
+        const unsigned char *st_nxt = stage_of(k_nxt);
 #pragma unroll
-            for (int p = 0; p < TB / 2; ++p) dd[p] = *reinterpret_cast<const float4 *>(du_c + (q * TB / 2 + p) * 4);
+        for (int q = 0; q < NSUB; ++q) {
+            const int i = sup * NSUB + q;  // i & 1 == q & 1: register slots are compile-time
+
+            uint32_t bcu[2][32];
+            if (ok) {
+                tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64, bcu[0]);
+                tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64 + 32, bcu[1]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) bcu[0][k] = bcu[1][k] = 0u;
+            }
+            tc::tmem_wait_ld_tied(bcu[0], bcu[1]);
+
+            // one block: y of sub-tile i-1, Delta etc. of sub-tile i+1, the recurrence of sub-tile i
+            float4 dq[TB / 2];
+#pragma unroll
+            for (int p = 0; p < TB / 2; ++p) dq[p] = sDU[((i & 1) * CH + c) * S + p];
+            output_pair(i - 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+            if (q + 1 < NSUB)
+                side_pair(st_cur, q + 1, i + 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+            else
+                side_pair(st_nxt, 0, i + 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
             float pq[TB];
 #pragma unroll
             for (int p = 0; p < TB / 2; ++p) {
-                const float2 dl = f2(dd[p].x, dd[p].y);
-                const float2 du = f2(dd[p].z, dd[p].w);
-                const float *bcp = bc + 16 * p;
+                const float2 dl = f2(dq[p].x, dq[p].y);
+                const float2 du = f2(dq[p].z, dq[p].w);
+                const uint32_t *bcp = bcu[p >> 1] + 16 * (p & 1);
                 float2 hp[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float2 x = __fmul2_rn(dl, A2d[j]);
-                    const float2 bu = __fmul2_rn(du, f2(bcp[2 * j], bcp[2 * j + 1]));
+                    const float2 bu = __fmul2_rn(du, f2(__uint_as_float(bcp[2 * j]), __uint_as_float(bcp[2 * j + 1])));
                     const float ht = fmaf(ex2_approx(x.x), h[j], bu.x);
                     h[j] = fmaf(ex2_approx(x.y), ht, bu.y);
                     hp[j] = f2(ht, h[j]);
                 }
                 if (MODE == MODE_FULL) {
-                    float2 P = __fmul2_rn(f2(bcp[8], bcp[9]), hp[0]);
-                    P = __ffma2_rn(f2(bcp[10], bcp[11]), hp[1], P);
-                    P = __ffma2_rn(f2(bcp[12], bcp[13]), hp[2], P);
-                    P = __ffma2_rn(f2(bcp[14], bcp[15]), hp[3], P);
+                    float2 P = __fmul2_rn(f2(__uint_as_float(bcp[8]), __uint_as_float(bcp[9])), hp[0]);
+                    P = __ffma2_rn(f2(__uint_as_float(bcp[10]), __uint_as_float(bcp[11])), hp[1], P);
+                    P = __ffma2_rn(f2(__uint_as_float(bcp[12]), __uint_as_float(bcp[13])), hp[2], P);
+                    P = __ffma2_rn(f2(__uint_as_float(bcp[14]), __uint_as_float(bcp[15])), hp[3], P);
                     pq[2 * p] = P.x;
                     pq[2 * p + 1] = P.y;
                 }
             }
             if (MODE == MODE_FULL) {
-#pragma unroll
-                for (int t = 0; t < TB; t += 4)
-                    *reinterpret_cast<float4 *>(prow + q * TB + t) = make_float4(pq[t], pq[t + 1], pq[t + 2], pq[t + 3]);
+                float *prow = sP + (((i & 1) * CH + c) * S + s) * Sh::P_STRIDE;
+                *reinterpret_cast<float4 *>(prow) = make_float4(pq[0], pq[1], pq[2], pq[3]);
+                *reinterpret_cast<float4 *>(prow + 4) = make_float4(pq[4], pq[5], pq[6], pq[7]);
             }
+            __syncwarp();  // partials of sub-tile i and Delta of sub-tile i+1 visible to the channel's lanes
         }
-        if (failed) break;
-
-        if (MODE == MODE_FULL) {
-            __syncwarp();
-            float2 ys[SEG / 2];
-#pragma unroll
-            for (int i = 0; i < SEG / 2; ++i) ys[i] = f2(0.f, 0.f);
-#pragma unroll
-            for (int r = 0; r < S; ++r) {
-                const float *pr = sP + (c * S + r) * Sh::P_STRIDE + s * SEG;
-#pragma unroll
-                for (int i = 0; i < SEG; i += 4) {
-                    const float4 v = *reinterpret_cast<const float4 *>(pr + i);
-                    ys[i / 2] = __fadd2_rn(ys[i / 2], f2(v.x, v.y));
-                    ys[i / 2 + 1] = __fadd2_rn(ys[i / 2 + 1], f2(v.z, v.w));
-                }
-            }
-            float yv[SEG];
-#pragma unroll
-            for (int i = 0; i < SEG; i += 2) {
-                const float2 u2 = f2(IO::get(ru[i / PER16], i % PER16), IO::get(ru[(i + 1) / PER16], (i + 1) % PER16));
-                float2 yy = __ffma2_rn(D2, u2, ys[i / 2]);
-                if (has_z)
-                    yy = gate2<FAST>(yy, f2(IO::get(rz[i / PER16], i % PER16),
-                                            IO::get(rz[(i + 1) / PER16], (i + 1) % PER16)));
-                yv[i] = yy.x;
-                yv[i + 1] = yy.y;
-            }
-            T *py = reinterpret_cast<T *>(a.y) + row + tseg;
-            if (seg_full) {
-#pragma unroll
-                for (int w = 0; w < W; ++w) stg16(py + w * PER16, IO::pack(yv + w * PER16));
-            } else if (valid) {
-#pragma unroll
-                for (int i = 0; i < SEG; ++i)
-                    if (tseg + i < t_end) IO::store(a.y, row + tseg + i, yv[i]);
-            }
-        }
-        if (has_next) {
-#pragma unroll
-            for (int w = 0; w < W; ++w) {
-                ru[w] = nu[w];
-                rd[w] = nd[w];
-                rz[w] = nz[w];
-            }
-        }
-        __syncwarp();
+        k_cur = k_nxt;
     }
 
-    if (failed) {
-        if (tid == 0) {
-            atomicOr(&g_device_error, 1u);
-            // give MMAs already issued a bounded chance to finish before TMEM is freed
-            tc::mbar_wait_bounded(&mbar[0], 0, kWaitPolls);
-            tc::mbar_wait_bounded(&mbar[1], 0, kWaitPolls);
-        }
-    } else if (MODE == MODE_STATES) {
+    output_pair(nsup * NSUB - 1, Du_r[1], g_r[1]);  // the last sub-tile is odd
+    if (MODE == MODE_STATES) {
         float sdt = sdt_acc;
 #pragma unroll
         for (int off = 1; off < S; off <<= 1) sdt += __shfl_xor_sync(0xffffffffu, sdt, off);
@@ -449,9 +445,22 @@ scan_tm_kernel(const ScanArgs a) {
 
     tc::fence_before_sync();
     __syncthreads();
+    if (tid == 0 && *abort_flag != 0) {
+        atomicOr(&g_device_error, 1u);
+        // the MMAs and loads this CTA started must finish before its TMEM and
+        // shared memory are released (each stage has at most its latest
+        // issued phase open)
+        if (mma_issued > 0) {
+            tc::umma_commit(done);
+            tc::mbar_wait_bounded(done, 0, kWaitPolls);
+        }
+        for (int sn = max(0, last_loaded - NST + 1); sn <= last_loaded; ++sn)
+            tc::mbar_wait_bounded(&io[sn % NST], (sn / NST) & 1, kWaitPolls);
+    }
+    __syncthreads();
     if (warp == 0) {
         tc::fence_after_sync();
-        tc::tmem_dealloc(tmem_base, Sh::TMEM_COLS);
+        tc::tmem_dealloc(*taddr_s, Sh::TMEM_COLS);
     }
 }
 
