@@ -16,8 +16,6 @@ namespace mamba {
 
 namespace {
 
-constexpr int kNwg = 3;  // warpgroups per CTA: 96 channels, one CTA per SM
-
 // cuTensorMapEncodeTiled, reached through the runtime's driver entry point so
 // that the library does not link the driver library itself
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -56,10 +54,42 @@ bool encode_3d(CUtensorMap *m, const void *ptr, bool bf16, long long inner, long
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T, int MODE>
-cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, long long Bsz, int grid_chunks, cudaStream_t st) {
-    using Sh = TmShape<T, MODE, kNwg>;
-    auto kern = scan_tm_kernel<T, MODE, kNwg>;
+int device_sms() {
+    static int cache[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    if (cache[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+// CTA width in warps (8 channels each).  One CTA runs per SM, so the time is
+// set by the number of waves times the work of one CTA; pick the width that
+// minimises waves x warps (wider on ties).
+int choose_warps(long long Bsz, long long Dch, int grid_chunks, int sms) {
+    using Sh = TmShape<float, MODE_FULL>;
+    int best = Sh::MAX_WARPS;
+    long long best_cost = -1;
+    for (int w = Sh::MAX_WARPS; w >= Sh::MIN_WARPS; --w) {
+        const long long ctas = Bsz * ((Dch + 8LL * w - 1) / (8LL * w)) * grid_chunks;
+        const long long waves = sms > 0 ? (ctas + sms - 1) / sms : 1;
+        const long long cost = waves * w;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = w;
+        }
+    }
+    return best;
+}
+
+template <typename T, int MODE, bool HAS_Z>
+cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int grid_chunks,
+                          cudaStream_t st) {
+    using Sh = TmShape<T, MODE>;
+    auto kern = scan_tm_kernel<T, MODE, HAS_Z>;
     static bool attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -69,9 +99,18 @@ cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, long long Bsz, 
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDevices) attr_set[dev] = true;
     }
-    dim3 grid((unsigned)((a.Dch + Sh::CH - 1) / Sh::CH), (unsigned)Bsz, (unsigned)grid_chunks);
-    kern<<<grid, Sh::NTHR, Sh::SMEM_BYTES, st>>>(a, maps);
+    const long long ch = 8LL * warps;
+    dim3 grid((unsigned)((a.Dch + ch - 1) / ch), (unsigned)Bsz, (unsigned)grid_chunks);
+    kern<<<grid, 32 * warps, Sh::SMEM_BYTES, st>>>(a, maps);
     return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_tm_t(int mode, const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int gc,
+                        cudaStream_t st) {
+    if (mode == MODE_STATES) return launch_tm_one<T, MODE_STATES, false>(a, maps, warps, Bsz, gc, st);
+    return a.z != nullptr ? launch_tm_one<T, MODE_FULL, true>(a, maps, warps, Bsz, gc, st)
+                          : launch_tm_one<T, MODE_FULL, false>(a, maps, warps, Bsz, gc, st);
 }
 
 }  // namespace
@@ -80,19 +119,17 @@ cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &a, long long Bsz
     // TMA coordinates are 32-bit: the time axis and the channel axis must fit
     if (a.L >= (1LL << 31) - 64 || a.Dch >= (1LL << 31) - 128 || Bsz >= (1LL << 31)) return cudaErrorNotSupported;
     const bool bf16 = dtype == 1;
-    constexpr int CH = 32 * kNwg;
+    const int warps = choose_warps(Bsz, a.Dch, grid_chunks, device_sms());
+    const unsigned ch = 8u * (unsigned)warps;
     TmMaps maps;
-    bool ok = encode_3d(&maps.u, a.u, bf16, a.L, a.Dch, Bsz, CH, true) &&
-              encode_3d(&maps.delta, a.delta, bf16, a.L, a.Dch, Bsz, CH, true) &&
-              encode_3d(&maps.z, a.z != nullptr ? a.z : a.u, bf16, a.L, a.Dch, Bsz, CH, true) &&
-              encode_3d(&maps.B, a.Bm, bf16, a.L, a.N, Bsz, 16, false) &&
-              encode_3d(&maps.C, a.Cm, bf16, a.L, a.N, Bsz, 16, false);
+    const bool ok = encode_3d(&maps.u, a.u, bf16, a.L, a.Dch, Bsz, ch, true) &&
+                    encode_3d(&maps.delta, a.delta, bf16, a.L, a.Dch, Bsz, ch, true) &&
+                    encode_3d(&maps.z, a.z != nullptr ? a.z : a.u, bf16, a.L, a.Dch, Bsz, ch, true) &&
+                    encode_3d(&maps.B, a.Bm, bf16, a.L, a.N, Bsz, 16, false) &&
+                    encode_3d(&maps.C, a.Cm, bf16, a.L, a.N, Bsz, 16, false);
     if (!ok) return cudaErrorNotSupported;
-    if (bf16)
-        return mode == MODE_FULL ? launch_tm_one<bf16_t, MODE_FULL>(a, maps, Bsz, grid_chunks, st)
-                                 : launch_tm_one<bf16_t, MODE_STATES>(a, maps, Bsz, grid_chunks, st);
-    return mode == MODE_FULL ? launch_tm_one<float, MODE_FULL>(a, maps, Bsz, grid_chunks, st)
-                             : launch_tm_one<float, MODE_STATES>(a, maps, Bsz, grid_chunks, st);
+    return bf16 ? launch_tm_t<bf16_t>(mode, a, maps, warps, Bsz, grid_chunks, st)
+                : launch_tm_t<float>(mode, a, maps, warps, Bsz, grid_chunks, st);
 }
 
 }  // namespace mamba

@@ -21,20 +21,21 @@
 // split into three bf16 parts hi+mid+lo whose fp32 sum reproduces it, K rows
 // 3s..3s+2).  D lands in TMEM as fp32; thread m reads its lane with
 // tcgen05.ld.  Pairing the columns by time lets the f32x2 instructions take
-// (Delta_t, Delta_t+1) against a duplicated (A_n, A_n) and (Delta u) pairs
-// against (B_n(t), B_n(t+1)) without register moves; the h recurrence stays
-// scalar.
+// (Delta_t, Delta_t+1) against a duplicated (A_n, A_n), (Delta u) pairs
+// against (B_n(t), B_n(t+1)) and (C_n(t), C_n(t+1)) against the state pair
+// (h_n(t), h_n(t+1)), which the recurrence writes in place.
 //
-// B and C do not depend on the channel, so every warpgroup of a CTA reads the
-// same TMEM columns: a CTA of NWG warpgroups (32 channels each, 4 lanes per
-// channel, lane m%4 owning states 4(m%4)..+3) takes the whole of TMEM (512
-// columns, one CTA per SM) as two buffers of one 32-step super-tile each.  Per
-// super-tile the CTA does, once: one MMA (M=128, N=256, K=16), five tiled TMA
-// loads (u, Delta_raw, z boxes of 32 steps x 32 NWG channels, B and C boxes of
-// 32 steps x 16 states; out-of-range rows and steps read as zero), one X build
-// and one CTA barrier.  The input ring has 3 stages, loaded two super-tiles
-// ahead; u/Delta_raw/z use the TMA's 16-byte-chunk swizzle so that the 8
-// channels of a warp hit distinct banks.
+// B and C do not depend on the channel, so all warps of a CTA read the same
+// TMEM columns: a CTA of W warps (8 channels each, 4 lanes per channel, lane
+// m%4 owning states 4(m%4)..+3; warp w reads TMEM lanes 32(w%4)..+31) takes the
+// whole of TMEM (512 columns, one CTA per SM) as two buffers of one 32-step
+// super-tile each.  W (8..12) is chosen per problem so that the CTAs fill the
+// SMs in whole waves.  Per super-tile the CTA does, once: one MMA (M=128,
+// N=256, K=16), five tiled TMA loads (u, Delta_raw, z boxes of 32 steps x 8W
+// channels, B and C boxes of 32 steps x 16 states; out-of-range rows and steps
+// read as zero), one X build and one CTA barrier.  The input ring has 3 stages,
+// loaded two super-tiles ahead; u/Delta_raw/z use the TMA's 16-byte-chunk
+// swizzle so that the 8 channels of a warp hit distinct banks.
 //
 // Per 8-step sub-tile i each lane loads its 64 TMEM columns, then in one
 // branch-free block computes Delta = softplus(.), Delta*u, D*u and SiLU(z) for
@@ -44,10 +45,10 @@
 // predicated store) and runs the recurrence over sub-tile i's 8 steps.
 //
 // Every mbarrier wait is bounded; a timeout sets a shared abort flag that
-// every later wait honours and that stops further loads, is recorded in the
-// device error word, and the CTA still walks its loop (no further MMAs or
-// TMEM loads), waits (bounded) for its issued MMAs and loads, frees its TMEM
-// and returns.
+// every later wait honours and that stops further loads and MMAs, is recorded
+// in the device error word, and the CTA still walks its loop (its results are
+// then meaningless), waits (bounded) for its issued MMAs and loads, frees its
+// TMEM and returns.
 #pragma once
 
 #include <cuda.h>
@@ -62,15 +63,16 @@ namespace mamba {
 // tensor-memory scan timed out.
 
 // TMA descriptors of one call: u, Delta_raw, z as [Bsz][Dch][L] with boxes of
-// 32 steps x CH channels (swizzled); B, C as [Bsz][N][L] with boxes of 32
+// 32 steps x 8W channels (swizzled); B, C as [Bsz][N][L] with boxes of 32
 // steps x 16 states (plain).
 struct TmMaps {
     CUtensorMap u, delta, z, B, C;
 };
 
-template <typename T, int MODE, int NWG>
+template <typename T, int MODE>
 struct TmShape {
-    static constexpr int NTHR = 128 * NWG, CH = 32 * NWG, S = 4;
+    static constexpr int MIN_WARPS = 8, MAX_WARPS = 12;  // CTA width, 8 channels per warp
+    static constexpr int MAX_THR = 32 * MAX_WARPS, MAX_CH = 8 * MAX_WARPS, S = 4;
     static constexpr int TT = 32;                  // steps per super-tile
     static constexpr int TB = 8;                   // steps per sub-tile
     static constexpr int NSUB = TT / TB;
@@ -80,14 +82,14 @@ struct TmShape {
     static constexpr bool SPLIT = sizeof(T) == 4;
     static constexpr int ROW = TT * (int)sizeof(T);  // bytes of one row of a box
     static constexpr int SWZ = ROW / 16;             // 16-byte chunks per swizzle span (64 B or 128 B)
-    static constexpr int IO_TILE = CH * ROW;         // one of u, Delta_raw, z
+    static constexpr int IO_TILE = MAX_CH * ROW;     // slot of one of u, Delta_raw, z (box: 8W rows)
     static constexpr int BC_TILE = 16 * ROW;         // one of B, C
     static constexpr int STAGE_BYTES = 3 * IO_TILE + 2 * BC_TILE;
     static constexpr int A_BYTES = 128 * 16 * 2;
     static constexpr int X_BYTES = COLS * 16 * 2;
-    static constexpr int DU_BYTES = CH * S * 16;           // per sub-tile: (Delta, Delta', du, du') per lane
-    static constexpr int P_STRIDE = TB + 4;                // floats per (channel, lane) row of partials
-    static constexpr int P_BYTES = CH * S * P_STRIDE * 4;  // per sub-tile
+    static constexpr int DU_BYTES = MAX_CH * S * 16;           // per sub-tile: (Delta, Delta', du, du') per lane
+    static constexpr int P_STRIDE = TB + 4;                    // floats per (channel, lane) row of partials
+    static constexpr int P_BYTES = MAX_CH * S * P_STRIDE * 4;  // per sub-tile
     static constexpr int OFF_ST = 0;
     static constexpr int OFF_A = OFF_ST + NST * STAGE_BYTES;
     static constexpr int OFF_X = OFF_A + A_BYTES;
@@ -100,13 +102,14 @@ struct TmShape {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
-template <typename T, int MODE, int NWG>
-__global__ void __launch_bounds__(128 * NWG, 1)
+// HAS_Z: the gate z is given (MODE_FULL only).  blockDim.x = 32 W, W in 8..12.
+template <typename T, int MODE, bool HAS_Z>
+__global__ void __launch_bounds__(TmShape<T, MODE>::MAX_THR, 1)
 scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
-    using Sh = TmShape<T, MODE, NWG>;
+    using Sh = TmShape<T, MODE>;
     constexpr bool FAST = sizeof(T) == 2;
-    constexpr int S = Sh::S, TT = Sh::TT, TB = Sh::TB, NSUB = Sh::NSUB, COLS = Sh::COLS, CH = Sh::CH;
-    constexpr int NST = Sh::NST, NTHR = Sh::NTHR;
+    constexpr int S = Sh::S, TT = Sh::TT, TB = Sh::TB, NSUB = Sh::NSUB, COLS = Sh::COLS, MAX_CH = Sh::MAX_CH;
+    constexpr int NST = Sh::NST;
     constexpr uint32_t kWaitPolls = 1u << 24;
     constexpr uint32_t kIdesc = tc::umma_idesc_bf16_f32(128, COLS);
     using Word = typename std::conditional<Sh::SPLIT, float2, uint32_t>::type;  // one step pair
@@ -116,8 +119,8 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     unsigned char *const sSt = smem + Sh::OFF_ST;
     uint16_t *const sA = reinterpret_cast<uint16_t *>(smem + Sh::OFF_A);
     unsigned char *const sX = smem + Sh::OFF_X;
-    float4 *const sDU = reinterpret_cast<float4 *>(smem + Sh::OFF_DU);  // [2][CH][S]
-    float *const sP = reinterpret_cast<float *>(smem + Sh::OFF_P);      // [2][CH][S][P_STRIDE]
+    float4 *const sDU = reinterpret_cast<float4 *>(smem + Sh::OFF_DU);  // [2][MAX_CH][S]
+    float *const sP = reinterpret_cast<float *>(smem + Sh::OFF_P);      // [2][MAX_CH][S][P_STRIDE]
     uint64_t *const full = reinterpret_cast<uint64_t *>(smem + Sh::OFF_BAR);  // [2] MMA of a super-tile done
     uint64_t *const xready = full + 2;                                        // X built by every warp
     uint64_t *const done = full + 3;                                          // abort path: all MMAs done
@@ -125,21 +128,21 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     uint32_t *const taddr_s = reinterpret_cast<uint32_t *>(smem + Sh::OFF_BAR + 64);
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(smem + Sh::OFF_BAR + 68);
 
+    const int nthr = blockDim.x, ch = nthr >> 2;  // channels of this CTA
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = tid & 3, c = tid >> 2;  // channel within the CTA, state slice
-    const long long d0 = (long long)blockIdx.x * CH;
+    const long long d0 = (long long)blockIdx.x * ch;
     const long long d = d0 + c;
     const bool valid = d < a.Dch;
     const long long b = blockIdx.y;
     const int kch = blockIdx.z;
     const long long N = a.N, L = a.L;
     const long long t_begin = (long long)kch * a.chunk_len;
-    const long long t_end = min(L, t_begin + a.chunk_len);
-    const int nsup = (int)((t_end - t_begin + TT - 1) / TT);
+    const int len = (int)(min(L, t_begin + a.chunk_len) - t_begin);  // steps of this chunk (< 2^31)
+    const int nsup = (len + TT - 1) / TT;
     const long long dd = valid ? d : 0;
-    const long long row = (b * a.Dch + dd) * L;
-    const bool has_z = a.z != nullptr;
-    const bool load_z = MODE == MODE_FULL && has_z;
+    // a step pair of this lane at offset r (from t_begin) is in range iff (unsigned) r < lenv
+    const unsigned lenv = valid ? (unsigned)len : 0u;
 
     // ---------------------------------------------------------------- one-time set-up
     if (warp == 0) {
@@ -147,26 +150,26 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         tc::tmem_relinquish();
     }
     // selector: element (m, k) of the 128 x 16 K-major operand
-    for (int i = tid; i < 128 * 16; i += NTHR) {
+    for (int i = tid; i < 128 * 16; i += nthr) {
         const int m = i >> 4, kk = i & 15;
         const bool one = Sh::SPLIT ? (kk < 12 && kk / 3 == (m & 3)) : (kk == (m & 3));
         sA[((m >> 3) * 256 + (kk >> 3) * 128 + (m & 7) * 16 + (kk & 7) * 2) >> 1] = one ? 0x3F80u : 0u;
     }
-    for (int i = tid; i < 2 * Sh::X_BYTES / 16; i += NTHR)
+    for (int i = tid; i < 2 * Sh::X_BYTES / 16; i += nthr)
         reinterpret_cast<uint4 *>(sX)[i] = make_uint4(0u, 0u, 0u, 0u);
     if (tid == 0) {
         tc::mbar_init(&full[0], 1);
         tc::mbar_init(&full[1], 1);
-        tc::mbar_init(xready, NTHR / 32);
+        tc::mbar_init(xready, nthr / 32);
         tc::mbar_init(done, 1);
         for (int k = 0; k < NST; ++k) tc::mbar_init(&io[k], 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
 
-    // per-lane constants and state (states n = 4s + j); A2d[j] = (A_n log2 e, A_n log2 e)
-    float2 A2d[4];
-    float h[4];
+    // per-lane constants and state (states n = 4s + j).  A2d[j] = (A_n log2 e, A_n log2 e);
+    // hh[j] = (h_n(t), h_n(t+1)) of the last step pair, .y the current state.
+    float2 A2d[4], hh[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const long long n = 4LL * s + j;
@@ -174,12 +177,15 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         if (valid && n < N) an = a.A[dd * N + n] * kLog2e;
         if (a.hin != nullptr && valid && n < N) hn = a.hin[((b * a.nchunks + kch) * a.Dch + dd) * N + n];
         A2d[j] = f2(an, an);
-        h[j] = hn;
+        hh[j] = f2(0.f, hn);
     }
     const float Dd = (a.D != nullptr && valid) ? a.D[dd] : 0.f;
     const float bias = (a.bias != nullptr && valid) ? a.bias[dd] : 0.f;
     const float2 bias2 = f2(bias, bias);
     const float2 D2 = f2(Dd, Dd);
+    const bool softplus = a.softplus != 0;
+    // y of the step at offset r from t_begin in this lane's channel: ylane + r
+    T *const ylane = reinterpret_cast<T *>(a.y) + ((b * a.Dch + dd) * L + t_begin);
 
     // bounded wait that gives up at once when another warp has already given up
     auto wait_or_abort = [&](uint64_t *bar, uint32_t parity) -> bool {
@@ -197,10 +203,10 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         unsigned char *st = stage_of(sn % NST);
         uint64_t *bar = &io[sn % NST];
         const int x = (int)(t_begin + (long long)sn * TT);
-        tc::mbar_arrive_expect_tx(bar, (uint32_t)((load_z ? 3 : 2) * Sh::IO_TILE + 2 * Sh::BC_TILE));
+        tc::mbar_arrive_expect_tx(bar, (uint32_t)((HAS_Z ? 3 : 2) * ch * Sh::ROW + 2 * Sh::BC_TILE));
         tc::tma_load_3d(st, &maps.u, x, (int)d0, (int)b, bar);
         tc::tma_load_3d(st + Sh::IO_TILE, &maps.delta, x, (int)d0, (int)b, bar);
-        if (load_z) tc::tma_load_3d(st + 2 * Sh::IO_TILE, &maps.z, x, (int)d0, (int)b, bar);
+        if (HAS_Z) tc::tma_load_3d(st + 2 * Sh::IO_TILE, &maps.z, x, (int)d0, (int)b, bar);
         tc::tma_load_3d(st + 3 * Sh::IO_TILE, &maps.B, x, 0, (int)b, bar);
         tc::tma_load_3d(st + 3 * Sh::IO_TILE + Sh::BC_TILE, &maps.C, x, 0, (int)b, bar);
     };
@@ -210,7 +216,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     auto x_build = [&](int xb, const unsigned char *st) {
         const T *raw = reinterpret_cast<const T *>(st + 3 * Sh::IO_TILE);  // [which][16][TT]
         unsigned char *xbase = sX + xb * Sh::X_BYTES;
-        for (int n = tid; n < COLS; n += NTHR) {
+        for (int n = tid; n < COLS; n += nthr) {
             const int j = n & 15;
             const int t = 2 * (n >> 4) + (j & 1);
             const int which = j >> 3, col = (j & 7) >> 1;
@@ -246,53 +252,55 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         }
     };
 
-    // ---- per-lane step pair (t0, t0 + 1) of sub-tile i, t0 = t_begin + 8 i + 2 s.
-    // t_end is even on the vectorised path, so a pair lies wholly inside or
-    // wholly outside [t_begin, t_end).
-    auto pair_t0 = [&](int i) { return t_begin + (long long)i * TB + 2 * s; };
+    // ---- this lane's step pair of sub-tile q of a stage: steps 8q + 2s, +1 of
+    // the super-tile.  The box rows are swizzled: byte offset o of the
+    // 1024-byte aligned box sits at o ^ (((o >> 7) % SWZ) << 4).
     auto unpack = [](Word w) -> float2 {
         if constexpr (Sh::SPLIT) return w;
         else return f2(bf16_lo(w), bf16_hi(w));
     };
-    // this lane's pair of sub-tile q of a stage; the box rows are swizzled:
-    // 16-byte chunk k of row r sits at chunk k ^ (r mod SWZ) ... of the
-    // 1024-byte aligned pattern, i.e. byte offset o -> o ^ (((o >> 7) % SWZ) << 4)
-    auto stage_word = [&](const unsigned char *st, int tensor, int q) -> Word {
+    int sw_off[NSUB];  // swizzled byte offset of this lane's pair in sub-tile q
+#pragma unroll
+    for (int q = 0; q < NSUB; ++q) {
         const int o = c * Sh::ROW + (q * TB + 2 * s) * (int)sizeof(T);
-        const int osw = o ^ (((o >> 7) & (Sh::SWZ - 1)) << 4);
-        return *reinterpret_cast<const Word *>(st + tensor * Sh::IO_TILE + osw);
+        sw_off[q] = o ^ (((o >> 7) & (Sh::SWZ - 1)) << 4);
+    }
+    auto stage_word = [&](const unsigned char *st, int tensor, int q) -> Word {
+        return *reinterpret_cast<const Word *>(st + tensor * Sh::IO_TILE + sw_off[q]);
     };
-    // Delta, Delta * u -> sDU[i & 1][c][s] (read by the channel's 4 lanes);
-    // D * u and SiLU(z) stay in this lane's registers until y of the pair is formed
+    float4 *const du_mine = sDU + c * S + s;  // + (i & 1) * MAX_CH * S
+    // Delta, Delta * u of this lane's pair at offset r (sub-tile parity par) ->
+    // sDU; D * u and SiLU(z) stay in this lane's registers until y of the pair is formed
     float sdt_acc = 0.f;  // MODE_STATES: this lane's share of sum(Delta) over the chunk
-    auto side_pair = [&](const unsigned char *st, int q, int i, float2 &Du, float2 &g) {
-        const bool in = valid && pair_t0(i) < t_end;
+    auto side_pair = [&](const unsigned char *st, int q, int r, int par, float2 &Du, float2 &g) {
+        const bool in = (unsigned)r < lenv;
         const float2 u = unpack(stage_word(st, 0, q));
         const float2 raw = __fadd2_rn(unpack(stage_word(st, 1, q)), bias2);
-        float2 dl = a.softplus ? softplus2<FAST>(raw) : raw;
-        float2 du = __fmul2_rn(dl, u);
-        if (!in) dl = du = f2(0.f, 0.f);
-        sDU[((i & 1) * CH + c) * S + s] = make_float4(dl.x, dl.y, du.x, du.y);
+        float2 dl = softplus ? softplus2<FAST>(raw) : raw;
+        dl = in ? dl : f2(0.f, 0.f);
+        const float2 du = __fmul2_rn(dl, u);  // zero outside the range: u there is finite box fill or data
+        du_mine[par * MAX_CH * S] = make_float4(dl.x, dl.y, du.x, du.y);
         if (MODE == MODE_STATES) sdt_acc += dl.x + dl.y;
         if (MODE == MODE_FULL) {
             Du = __fmul2_rn(D2, u);
-            g = has_z ? silu2<FAST>(unpack(stage_word(st, 2, q))) : f2(1.f, 1.f);
+            if (HAS_Z) g = silu2<FAST>(unpack(stage_word(st, 2, q)));
         }
     };
-    // y of this lane's step pair of sub-tile i from the channel's 4 partial sums
-    auto output_pair = [&](int i, float2 Du, float2 g) {
+    const float *const p_mine = sP + (c * S) * Sh::P_STRIDE + 2 * s;  // + (i & 1) * MAX_CH * S * P_STRIDE
+    // y of this lane's pair at offset r from the channel's 4 partial sums
+    auto output_pair = [&](int r, int par, float2 Du, float2 g) {
         if (MODE != MODE_FULL) return;
-        const float *pp = sP + ((i & 1) * CH + c) * S * Sh::P_STRIDE + 2 * s;
+        const float *pp = p_mine + par * MAX_CH * S * Sh::P_STRIDE;
         float2 ys = *reinterpret_cast<const float2 *>(pp);
 #pragma unroll
-        for (int r = 1; r < S; ++r) ys = __fadd2_rn(ys, *reinterpret_cast<const float2 *>(pp + r * Sh::P_STRIDE));
-        const float2 yy = __fmul2_rn(__fadd2_rn(ys, Du), g);
-        const long long t0 = pair_t0(i);
-        const bool st = valid && t0 >= t_begin && t0 < t_end;
+        for (int k = 1; k < S; ++k) ys = __fadd2_rn(ys, *reinterpret_cast<const float2 *>(pp + k * Sh::P_STRIDE));
+        float2 yy = __fadd2_rn(ys, Du);
+        if (HAS_Z) yy = __fmul2_rn(yy, g);
+        const bool st = (unsigned)r < lenv;
         if constexpr (Sh::SPLIT)
-            st_f32x2_if(reinterpret_cast<float *>(a.y) + row + t0, yy, st);
+            st_f32x2_if(ylane + r, yy, st);
         else
-            st_b32_if(reinterpret_cast<uint16_t *>(a.y) + row + t0, pack_bf16x2(yy.x, yy.y), st);
+            st_b32_if(ylane + r, pack_bf16x2(yy.x, yy.y), st);
     };
 
     const uint64_t descA = tc::umma_desc(tc::smem_addr(sA), 128, 256);
@@ -327,7 +335,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     }
     // (D u, SiLU z) of the step pairs whose y is still open, by sub-tile parity
     float2 Du_r[2], g_r[2];
-    side_pair(stage_of(0), 0, 0, Du_r[0], g_r[0]);
+    side_pair(stage_of(0), 0, 2 * s, 0, Du_r[0], g_r[0]);
     __syncwarp();
 
     int k_cur = 0;  // stage of super-tile sup
@@ -358,61 +366,54 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                 }
             }
         }
-        // this super-tile's B/C are in TMEM buffer sup & 1
-        const bool ok = __all_sync(0xffffffffu, wait_or_abort(&full[sup & 1], (sup >> 1) & 1));
+        // this super-tile's B/C are in TMEM buffer sup & 1 (after an abort the
+        // loads below still read allocated TMEM; the results are then discarded)
+        if (!__all_sync(0xffffffffu, wait_or_abort(&full[sup & 1], (sup >> 1) & 1))) *abort_flag = 1;
         tc::fence_after_sync();
-        if (!ok) *abort_flag = 1;
         const unsigned char *st_cur = stage_of(k_cur);
         const unsigned char *st_nxt = stage_of(k_nxt);
+        const int r0 = sup * TT + 2 * s;  // this lane's pair offset in sub-tile 0 of this super-tile
 #pragma unroll
         for (int q = 0; q < NSUB; ++q) {
-            const int i = sup * NSUB + q;  // i & 1 == q & 1: register slots are compile-time
-
             uint32_t bcu[2][32];
-            if (ok) {
-                tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64, bcu[0]);
-                tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64 + 32, bcu[1]);
-            } else {
-#pragma unroll
-                for (int k = 0; k < 32; ++k) bcu[0][k] = bcu[1][k] = 0u;
-            }
+            tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64, bcu[0]);
+            tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64 + 32, bcu[1]);
             tc::tmem_wait_ld_tied(bcu[0], bcu[1]);
 
-            // one block: y of sub-tile i-1, Delta etc. of sub-tile i+1, the recurrence of sub-tile i
+            // one block: y of sub-tile i-1, Delta etc. of sub-tile i+1, the
+            // recurrence of sub-tile i (i = 4 sup + q, so i & 1 == q & 1)
             float4 dq[TB / 2];
 #pragma unroll
-            for (int p = 0; p < TB / 2; ++p) dq[p] = sDU[((i & 1) * CH + c) * S + p];
-            output_pair(i - 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+            for (int p = 0; p < TB / 2; ++p) dq[p] = du_mine[(q & 1) * MAX_CH * S - s + p];
+            output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
             if (q + 1 < NSUB)
-                side_pair(st_cur, q + 1, i + 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+                side_pair(st_cur, q + 1, r0 + (q + 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
             else
-                side_pair(st_nxt, 0, i + 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+                side_pair(st_nxt, 0, r0 + TT, 0, Du_r[0], g_r[0]);
             float pq[TB];
 #pragma unroll
             for (int p = 0; p < TB / 2; ++p) {
                 const float2 dl = f2(dq[p].x, dq[p].y);
                 const float2 du = f2(dq[p].z, dq[p].w);
                 const uint32_t *bcp = bcu[p >> 1] + 16 * (p & 1);
-                float2 hp[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const float2 x = __fmul2_rn(dl, A2d[j]);
                     const float2 bu = __fmul2_rn(du, f2(__uint_as_float(bcp[2 * j]), __uint_as_float(bcp[2 * j + 1])));
-                    const float ht = fmaf(ex2_approx(x.x), h[j], bu.x);
-                    h[j] = fmaf(ex2_approx(x.y), ht, bu.y);
-                    hp[j] = f2(ht, h[j]);
+                    hh[j].x = fmaf(ex2_approx(x.x), hh[j].y, bu.x);
+                    hh[j].y = fmaf(ex2_approx(x.y), hh[j].x, bu.y);
                 }
                 if (MODE == MODE_FULL) {
-                    float2 P = __fmul2_rn(f2(__uint_as_float(bcp[8]), __uint_as_float(bcp[9])), hp[0]);
-                    P = __ffma2_rn(f2(__uint_as_float(bcp[10]), __uint_as_float(bcp[11])), hp[1], P);
-                    P = __ffma2_rn(f2(__uint_as_float(bcp[12]), __uint_as_float(bcp[13])), hp[2], P);
-                    P = __ffma2_rn(f2(__uint_as_float(bcp[14]), __uint_as_float(bcp[15])), hp[3], P);
+                    float2 P = __fmul2_rn(f2(__uint_as_float(bcp[8]), __uint_as_float(bcp[9])), hh[0]);
+                    P = __ffma2_rn(f2(__uint_as_float(bcp[10]), __uint_as_float(bcp[11])), hh[1], P);
+                    P = __ffma2_rn(f2(__uint_as_float(bcp[12]), __uint_as_float(bcp[13])), hh[2], P);
+                    P = __ffma2_rn(f2(__uint_as_float(bcp[14]), __uint_as_float(bcp[15])), hh[3], P);
                     pq[2 * p] = P.x;
                     pq[2 * p + 1] = P.y;
                 }
             }
             if (MODE == MODE_FULL) {
-                float *prow = sP + (((i & 1) * CH + c) * S + s) * Sh::P_STRIDE;
+                float *prow = const_cast<float *>(p_mine) - 2 * s + s * Sh::P_STRIDE + (q & 1) * MAX_CH * S * Sh::P_STRIDE;
                 *reinterpret_cast<float4 *>(prow) = make_float4(pq[0], pq[1], pq[2], pq[3]);
                 *reinterpret_cast<float4 *>(prow + 4) = make_float4(pq[4], pq[5], pq[6], pq[7]);
             }
@@ -421,7 +422,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         k_cur = k_nxt;
     }
 
-    output_pair(nsup * NSUB - 1, Du_r[1], g_r[1]);  // the last sub-tile is odd
+    output_pair((nsup - 1) * TT + 3 * TB + 2 * s, 1, Du_r[1], g_r[1]);  // the last sub-tile is odd
     if (MODE == MODE_STATES) {
         float sdt = sdt_acc;
 #pragma unroll
@@ -431,7 +432,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const long long n = 4LL * s + j;
-                if (n < N) a.ws_h[base * N + n] = h[j];
+                if (n < N) a.ws_h[base * N + n] = hh[j].y;
             }
             if (s == 0) a.ws_sdt[base] = sdt;
         }
@@ -439,7 +440,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             const long long n = 4LL * s + j;
-            if (n < N) a.last_state[(b * a.Dch + d) * N + n] = h[j];
+            if (n < N) a.last_state[(b * a.Dch + d) * N + n] = hh[j].y;
         }
     }
 
