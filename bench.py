@@ -396,7 +396,8 @@ def bench_scan(args, m, torch):
     mufu_peak = SM_COUNT_NOMINAL * mufu_units * peaks["sm_max_mhz"] * 1e6   # ex2 per second
     t_mufu = exps / mufu_peak
     t_meas = t_ms * 1e-3
-    kernel = "scan_kernel<bf16,NP16,full>" if io == "bf16" and N <= 16 else f"scan_kernel<{io},N{N},full>"
+    tm = 8 < N <= 16 and os.environ.get("MAMBA_SCAN_KERNEL") != "smem"
+    kernel = (f"scan_tm_kernel<{io},full,z>" if tm else f"scan_kernel<{io},NP{1 << max(2, (N - 1).bit_length())},full>")
     traffic = traffic_record(f"{args.workload}")
     if t_mufu >= t_hbm:
         roof = {"bound": "alu", "achieved": round(exps / t_meas / 1e12, 4),
