@@ -249,18 +249,9 @@ def main():
     else:
         res = bench_scan(args, m, torch)
 
-    # max over ranks of the timed region
-    t_ms = res["ms_per_step"]
-    if dist is not None:
-        tt = torch.tensor([t_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_ms = float(tt.item())
-        te = torch.tensor([res["e2e_ms"]], device="cuda")
-        dist.all_reduce(te, op=dist.ReduceOp.MAX)
-        res["e2e_ms"] = float(te.item())
-    bytes_step = res["bytes"]
-    value = world * bytes_step / (t_ms * 1e-3) / 1e9
-    e2e_value = world * bytes_step / (res["e2e_ms"] * 1e-3) / 1e9
+    # max over ranks of the timed regions; every rank ran the same per-rank workload (weak scaling)
+    t_ms, res["e2e_ms"] = max_over_ranks([res["ms_per_step"], res["e2e_ms"]], dist, torch, "cuda")
+    value, e2e_value = aggregate_gbs(world, res["bytes"], t_ms, res["e2e_ms"])
     peaks = measured_peaks()
 
     cpu = None
@@ -293,6 +284,20 @@ def main():
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def max_over_ranks(values, dist, torch, device):
+    """Element-wise maximum over all ranks (the identity without a process group)."""
+    if dist is None:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def aggregate_gbs(world, bytes_per_rank_step, t_ms, e2e_ms):
+    """Whole-job GB/s: every rank moves bytes_per_rank_step per step; the slowest rank sets the time."""
+    return (world * bytes_per_rank_step / (t_ms * 1e-3) / 1e9, world * bytes_per_rank_step / (e2e_ms * 1e-3) / 1e9)
 
 
 def traffic_record(kernel_key):
