@@ -109,7 +109,9 @@ int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A, c
  *   h0          [Bsz][Dch][N] fp32 initial state (NULL = zero).  With
  *               MAMBA_FLAG_REVERSE it is the state "after" t = L, i.e. the
  *               state the backward-in-time scan starts from.
- *   flags       MAMBA_FLAG_ZOH | MAMBA_FLAG_REVERSE (0 = plain forward scan)
+ *   flags       MAMBA_FLAG_ZOH | MAMBA_FLAG_REVERSE (0 = plain forward scan);
+ *               a call with flags runs the general scalar-load kernel, which is
+ *               slower than the plain forward scan's kernels
  *   chunk_len   0: automatic choice between the direct and the chunked scan;
  *               > 0: force the chunked scan with chunks of this many steps
  *                    (rounded up to the kernel's time tile);

@@ -118,7 +118,6 @@ int scan_impl(const void *u, const void *delta, const float *A, const void *B, c
     int st = check_sizes(Bsz, Dch, L, N, dtype);
     if (st != MAMBA_OK) return st;
     if (flags & ~(MAMBA_FLAG_ZOH | MAMBA_FLAG_REVERSE)) return MAMBA_ERR_BAD_FLAGS;
-    if (flags != 0) return MAMBA_ERR_BAD_FLAGS;  // not implemented in this build of the kernels
 
     Plan plan;
     st = make_plan(Bsz, Dch, L, N, chunk_len, &plan);
@@ -142,6 +141,7 @@ int scan_impl(const void *u, const void *delta, const float *A, const void *B, c
     a.L = L;
     a.N = N;
     a.softplus = softplus_flag ? 1 : 0;
+    a.flags = flags;
 
     if (plan.K == 1) {
         a.hin = h0;

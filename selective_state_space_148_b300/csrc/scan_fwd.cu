@@ -31,11 +31,11 @@ ScanGeom scan_geom(long long N) {
     return geom_of<64>();
 }
 
-template <typename T, int NP, int MODE, bool VEC>
+template <typename T, int NP, int MODE, bool VEC, bool GEN = false>
 static cudaError_t launch_one(const ScanArgs &a, long long Bsz, int grid_chunks, cudaStream_t st) {
     using C = Cfg<NP>;
     using Sh = ScanShape<NP, C::NS, C::TT, C::NWARPS, MODE, (int)sizeof(T)>;
-    auto kern = scan_kernel<T, NP, C::NS, C::TT, C::NWARPS, MODE, VEC>;
+    auto kern = scan_kernel<T, NP, C::NS, C::TT, C::NWARPS, MODE, VEC, GEN>;
     if (Sh::SMEM_BYTES > 48 * 1024) {
         // opt in to more than 48 KB of dynamic shared memory, once per device
         static bool attr_set[kMaxDevices] = {};
@@ -55,6 +55,9 @@ static cudaError_t launch_one(const ScanArgs &a, long long Bsz, int grid_chunks,
 
 template <typename T, int NP>
 static cudaError_t launch_np(int mode, bool vec, const ScanArgs &a, long long Bsz, int gc, cudaStream_t st) {
+    if (a.flags != 0)  // ZOH and/or reverse: the general instantiation
+        return mode == MODE_FULL ? launch_one<T, NP, MODE_FULL, false, true>(a, Bsz, gc, st)
+                                 : launch_one<T, NP, MODE_STATES, false, true>(a, Bsz, gc, st);
     if (mode == MODE_FULL)
         return vec ? launch_one<T, NP, MODE_FULL, true>(a, Bsz, gc, st) : launch_one<T, NP, MODE_FULL, false>(a, Bsz, gc, st);
     return vec ? launch_one<T, NP, MODE_STATES, true>(a, Bsz, gc, st) : launch_one<T, NP, MODE_STATES, false>(a, Bsz, gc, st);
@@ -87,7 +90,8 @@ cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long l
                         cudaStream_t st) {
     // (its TMA boxes start on 32-step boundaries: chunks must be whole super-tiles;
     // it declines, with cudaErrorNotSupported, problems its descriptors cannot express)
-    if (vec && a.N > 8 && a.N <= 16 && (a.nchunks == 1 || a.chunk_len % 32 == 0) && use_tmem_kernel()) {
+    if (vec && a.flags == 0 && a.N > 8 && a.N <= 16 && (a.nchunks == 1 || a.chunk_len % 32 == 0) &&
+        use_tmem_kernel()) {
         const cudaError_t e = launch_scan_tm(dtype, mode, a, Bsz, grid_chunks, st);
         if (e != cudaErrorNotSupported) return e;
     }

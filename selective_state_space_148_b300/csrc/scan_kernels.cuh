@@ -49,7 +49,29 @@ struct ScanArgs {
     long long chunk_len;  // steps per chunk (multiple of TT); L for the direct scan
     int nchunks;          // K
     int softplus;
+    int flags;            // MAMBA_FLAG_ZOH (1) | MAMBA_FLAG_REVERSE (2); honoured by the GEN instantiation only
 };
+
+enum { SCAN_FLAG_ZOH = 1, SCAN_FLAG_REVERSE = 2 };
+
+// Exact zero-order-hold weight f = (e^{Delta A} - 1) / A (Delta where A = 0)
+// (freeguideonline tutorial §2.2: B_bar = (Delta A)^{-1} (exp(Delta A) - I) Delta B,
+// which for a diagonal A is (exp(Delta A_n) - 1) / A_n B_n).  e = 2^{x2} is
+// the decay already computed from x2 = Delta A log2 e.  e - 1 cancels for small
+// |Delta A|, so there expm1 is the Taylor series to the x^7 term (truncation
+// below 2e-7 relative for |x| < 1/2).  inv_a = 1/A_n (0 where A_n = 0), a_zero =
+// 1 where A_n = 0 (0 elsewhere).
+__device__ __forceinline__ float zoh_weight(float e, float x2, float dl, float inv_a, float a_zero) {
+    const float x = x2 * kLn2;
+    float p = fmaf(x, 1.0f / 5040.0f, 1.0f / 720.0f);
+    p = fmaf(x, p, 1.0f / 120.0f);
+    p = fmaf(x, p, 1.0f / 24.0f);
+    p = fmaf(x, p, 1.0f / 6.0f);
+    p = fmaf(x, p, 0.5f);
+    p = fmaf(x, p, 1.0f);
+    const float em1 = fabsf(x) < 0.5f ? x * p : e - 1.0f;
+    return fmaf(a_zero, dl, em1 * inv_a);
+}
 
 template <int NP, int NS, int TT, int NWARPS, int MODE, int IOBYTES>
 struct ScanShape {
@@ -75,7 +97,10 @@ struct ScanShape {
     static_assert(SEG % 4 == 0, "lane segment must be a multiple of 4 steps");
 };
 
-template <typename T, int NP, int NS, int TT, int NWARPS, int MODE, bool VEC>
+// GEN: the general instantiation (scalar loads only, VEC = false) that honours
+// a.flags: ZOH weights, and the reverse scan, which walks logical step tau at
+// physical index L - 1 - tau (chunks, carries and h0 are all in logical order).
+template <typename T, int NP, int NS, int TT, int NWARPS, int MODE, bool VEC, bool GEN = false>
 __global__ void __launch_bounds__(NWARPS * 32)
 scan_kernel(const ScanArgs a) {
     using Sh = ScanShape<NP, NS, TT, NWARPS, MODE, (int)sizeof(T)>;
@@ -104,10 +129,15 @@ scan_kernel(const ScanArgs a) {
     const long long row = (b * a.Dch + dd) * L;  // element offset of this channel's time row
     const long long bc_row0 = b * N * L;         // B/C rows of batch b
     const bool has_z = a.z != nullptr;
+    static_assert(!(GEN && VEC), "the general instantiation uses scalar loads");
+    const bool rev = GEN && (a.flags & SCAN_FLAG_REVERSE);
+    const bool zoh = GEN && (a.flags & SCAN_FLAG_ZOH);
+    auto ph = [&](long long t) { return rev ? (L - 1 - t) : t; };  // physical index of logical step t
 
     // ---- per-lane constants and state (states n = s*NS + j)
     float2 A2[NS / 2];  // A * log2(e), so A_bar = 2^(Delta * A2)
     float2 h[NS / 2];
+    float2 invA[GEN ? NS / 2 : 1], aZero[GEN ? NS / 2 : 1];  // ZOH: 1/A (0 at A = 0), [A = 0]
 #pragma unroll
     for (int j = 0; j < NS; j += 2) {
         const long long n0 = (long long)s * NS + j;
@@ -121,6 +151,10 @@ scan_kernel(const ScanArgs a) {
         }
         A2[j / 2] = make_float2(a0, a1);
         h[j / 2] = make_float2(h0, h1);
+        if constexpr (GEN) {
+            invA[j / 2] = make_float2(a0 != 0.f ? kLog2e / a0 : 0.f, a1 != 0.f ? kLog2e / a1 : 0.f);
+            aZero[j / 2] = make_float2(a0 == 0.f ? 1.f : 0.f, a1 == 0.f ? 1.f : 0.f);
+        }
     }
     const float Dd = (a.D != nullptr && valid) ? a.D[dd] : 0.f;
     const float bias = (a.bias != nullptr && valid) ? a.bias[dd] : 0.f;
@@ -143,13 +177,13 @@ scan_kernel(const ScanArgs a) {
                     const long long n = 4LL * g + j;
                     uint4 v = make_uint4(0u, 0u, 0u, 0u);
                     if (n < N) {
-                        const long long off = bc_row0 + n * L + tt;
+                        const long long off = bc_row0 + n * L;
                         if (VEC && tt + TPT <= t_end) {
-                            v = ldg16(reinterpret_cast<const T *>(base) + off);
+                            v = ldg16(reinterpret_cast<const T *>(base) + off + tt);
                         } else {
 #pragma unroll
                             for (int i = 0; i < TPT; ++i)
-                                if (tt + i < t_end) IO::set(v, i, IO::load(base, off + i));
+                                if (tt + i < t_end) IO::set(v, i, IO::load(base, off + ph(tt + i)));
                         }
                     }
                     rbc[m][j] = v;
@@ -197,9 +231,9 @@ scan_kernel(const ScanArgs a) {
                 for (int i = 0; i < PER16; ++i) {
                     const long long t = t0 + w * PER16 + i;
                     if (valid && t < t_end) {
-                        IO::set(vu, i, IO::load(a.u, row + t));
-                        IO::set(vd, i, IO::load(a.delta, row + t));
-                        if (has_z) IO::set(vz, i, IO::load(a.z, row + t));
+                        IO::set(vu, i, IO::load(a.u, row + ph(t)));
+                        IO::set(vd, i, IO::load(a.delta, row + ph(t)));
+                        if (has_z) IO::set(vz, i, IO::load(a.z, row + ph(t)));
                     }
                 }
                 xu[w] = vu;
@@ -240,7 +274,9 @@ scan_kernel(const ScanArgs a) {
                     float dl = a.softplus ? softplus_f(raw) : raw;
                     if (!(valid && t0 + ii < t_end)) dl = 0.f;  // masked step: state unchanged
                     o[2 * e] = dl;
-                    o[2 * e + 1] = dl * IO::get(ru[ii / PER16], ii % PER16);
+                    // ZOH keeps u itself: its weight depends on the state
+                    o[2 * e + 1] = zoh ? (dl != 0.f ? IO::get(ru[ii / PER16], ii % PER16) : 0.f)
+                                       : dl * IO::get(ru[ii / PER16], ii % PER16);
                     sdt_acc += dl;
                 }
                 *reinterpret_cast<float4 *>(du_row + (s * SEG + i) * 2) = make_float4(o[0], o[1], o[2], o[3]);
@@ -271,8 +307,20 @@ scan_kernel(const ScanArgs a) {
                         const float2 x23 = __fmul2_rn(dl2, A2[2 * g + 1]);
                         const float2 a01 = make_float2(ex2_approx(x01.x), ex2_approx(x01.y));
                         const float2 a23 = make_float2(ex2_approx(x23.x), ex2_approx(x23.y));
-                        const float2 bu01 = __fmul2_rn(du2v, make_float2(Bv.x, Bv.y));
-                        const float2 bu23 = __fmul2_rn(du2v, make_float2(Bv.z, Bv.w));
+                        float2 bu01 = __fmul2_rn(du2v, make_float2(Bv.x, Bv.y));
+                        float2 bu23 = __fmul2_rn(du2v, make_float2(Bv.z, Bv.w));
+                        if constexpr (GEN) {
+                            if (zoh) {  // du2v holds u: B_bar u = f_n u B_n
+                                const float2 iA01 = invA[2 * g], iA23 = invA[2 * g + 1];
+                                const float2 z01 = aZero[2 * g], z23 = aZero[2 * g + 1];
+                                const float2 f01 = make_float2(zoh_weight(a01.x, x01.x, dl, iA01.x, z01.x),
+                                                               zoh_weight(a01.y, x01.y, dl, iA01.y, z01.y));
+                                const float2 f23 = make_float2(zoh_weight(a23.x, x23.x, dl, iA23.x, z23.x),
+                                                               zoh_weight(a23.y, x23.y, dl, iA23.y, z23.y));
+                                bu01 = __fmul2_rn(__fmul2_rn(f01, du2v), make_float2(Bv.x, Bv.y));
+                                bu23 = __fmul2_rn(__fmul2_rn(f23, du2v), make_float2(Bv.z, Bv.w));
+                            }
+                        }
                         h[2 * g] = __ffma2_rn(a01, h[2 * g], bu01);
                         h[2 * g + 1] = __ffma2_rn(a23, h[2 * g + 1], bu23);
                         if (MODE == MODE_FULL) {
@@ -324,7 +372,7 @@ scan_kernel(const ScanArgs a) {
             } else if (valid) {
 #pragma unroll
                 for (int i = 0; i < SEG; ++i)
-                    if (t0 + i < t_end) IO::store(a.y, row + t0 + i, yv[i]);
+                    if (t0 + i < t_end) IO::store(a.y, row + ph(t0 + i), yv[i]);
             }
         }
 

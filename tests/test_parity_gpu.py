@@ -244,3 +244,69 @@ def test_full_workload_sampled(name):
     # properties that hold everywhere: finite outputs
     assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
     print(f"{name}: y err ratio {ey:.3g}, state {eh:.3g}, chunked={m.mamba_scan_workspace_size(Bsz, Dch, L, N) > 0}")
+
+
+# ----------------------------------------------------------------------------- flags: exact ZOH, reverse scan
+
+FLAG_CASES = {  # name -> (flags, oracle disc, oracle reverse)
+    "zoh": (0x1, 1, False),
+    "reverse": (0x2, 0, True),
+    "zoh_reverse": (0x3, 1, True),
+}
+
+
+@pytest.mark.parametrize("case", sorted(FLAG_CASES))
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("N", [4, 16, 33, 64])
+def test_flags_direct(case, io, N):
+    flags, disc, rev = FLAG_CASES[case]
+    x = inputs.make_scan_inputs(2, 21, N, 300, io=io, seed=20 + N)
+    h0 = np.random.default_rng(N).normal(0, 0.3, (2, 21, N)).astype(np.float32)
+    for h in (None, h0):
+        yg, hg = run_gpu(x, h0=h, flags=flags, chunk_len=-1)
+        yr, hr = run_oracle(x, h0=None if h is None else h.astype(np.float64), disc=disc, reverse=rev)
+        assert_close(yg, yr, TOL_Y[io], f"{case} N={N} {io} y")
+        assert_close(hg, hr, TOL_STATE, f"{case} N={N} {io} last_state")
+
+
+@pytest.mark.parametrize("case", sorted(FLAG_CASES))
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_flags_chunked(case, io):
+    flags, disc, rev = FLAG_CASES[case]
+    x = inputs.make_scan_inputs(1, 13, 16, 1000, io=io, seed=31)
+    h0 = np.random.default_rng(5).normal(0, 0.3, (1, 13, 16)).astype(np.float32)
+    yg, hg = run_gpu(x, h0=h0, flags=flags, chunk_len=128)
+    yr, hr = run_oracle(x, h0=h0.astype(np.float64), disc=disc, reverse=rev)
+    assert_close(yg, yr, TOL_Y[io], f"chunked {case} {io} y")
+    assert_close(hg, hr, TOL_STATE, f"chunked {case} {io} last_state")
+
+
+def test_zoh_with_a_zero_state():
+    """A state with A = 0 takes the limit Delta * B of the ZOH weight."""
+    x = inputs.make_scan_inputs(1, 9, 16, 200, io="f32", seed=33)
+    x.A = x.A.copy()
+    x.A[:, 3] = 0.0
+    x.A[4, :] = 0.0
+    yg, hg = run_gpu(x, flags=0x1, chunk_len=-1)
+    yr, hr = run_oracle(x, disc=1)
+    assert_close(yg, yr, TOL_Y["f32"], "zoh A=0 y")
+    assert_close(hg, hr, TOL_STATE, "zoh A=0 last_state")
+
+
+def test_flags_unaligned_and_ragged():
+    """Flagged calls take scalar loads everywhere: odd L and offset views."""
+    import torch
+    x = inputs.make_scan_inputs(2, 11, 16, 97, io="bf16", seed=34)
+    t = dev_inputs(x)
+    big = {k: torch.empty(v.numel() + 1, dtype=v.dtype, device="cuda") for k, v in t.items() if k in ("u", "delta", "z")}
+    for k, v in big.items():
+        v[1:].copy_(t[k].reshape(-1))
+        t[k] = v[1:].view(t[k].shape)
+    y = torch.empty_like(t["u"])
+    last = torch.empty((2, 11, 16), dtype=torch.float32, device="cuda")
+    m.mamba_selective_scan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], 1,
+                                  y, last, flags=0x3, chunk_len=-1)
+    torch.cuda.synchronize()
+    yr, hr = run_oracle(x, disc=1, reverse=True)
+    assert_close(to_host_f64(y), yr, TOL_Y["bf16"], "flags unaligned y")
+    assert_close(last.cpu().numpy().astype(np.float64), hr, TOL_STATE, "flags unaligned last_state")
