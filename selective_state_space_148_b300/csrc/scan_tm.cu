@@ -66,15 +66,16 @@ int device_sms() {
     return cache[dev];
 }
 
-// CTA width in warps (8 channels each).  One CTA runs per SM, so the time is
-// set by the number of waves times the work of one CTA; pick the width that
-// minimises waves x warps (wider on ties).
-int choose_warps(long long Bsz, long long Dch, int grid_chunks, int sms) {
+// CTA width in warps (32 / S channels each).  One CTA runs per SM, so the
+// time is set by the number of waves times the work of one CTA; pick the width
+// that minimises waves x warps (wider on ties).
+int choose_warps(long long Bsz, long long Dch, int grid_chunks, int sms, int S) {
     using Sh = TmShape<float, MODE_FULL>;
     int best = Sh::MAX_WARPS;
     long long best_cost = -1;
     for (int w = Sh::MAX_WARPS; w >= Sh::MIN_WARPS; --w) {
-        const long long ctas = Bsz * ((Dch + 8LL * w - 1) / (8LL * w)) * grid_chunks;
+        const long long cw = 32LL * w / S;  // channels per CTA
+        const long long ctas = Bsz * ((Dch + cw - 1) / cw) * grid_chunks;
         const long long waves = sms > 0 ? (ctas + sms - 1) / sms : 1;
         const long long cost = waves * w;
         if (best_cost < 0 || cost < best_cost) {
@@ -85,11 +86,11 @@ int choose_warps(long long Bsz, long long Dch, int grid_chunks, int sms) {
     return best;
 }
 
-template <typename T, int MODE, bool HAS_Z>
+template <typename T, int MODE, bool HAS_Z, int S>
 cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int grid_chunks,
                           cudaStream_t st) {
-    using Sh = TmShape<T, MODE>;
-    auto kern = scan_tm_kernel<T, MODE, HAS_Z>;
+    using Sh = TmShape<T, MODE, S>;
+    auto kern = scan_tm_kernel<T, MODE, HAS_Z, S>;
     static bool attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -99,18 +100,18 @@ cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, int warps, long
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < kMaxDevices) attr_set[dev] = true;
     }
-    const long long ch = 8LL * warps;
+    const long long ch = 32LL * warps / S;
     dim3 grid((unsigned)((a.Dch + ch - 1) / ch), (unsigned)Bsz, (unsigned)grid_chunks);
     kern<<<grid, 32 * warps, Sh::SMEM_BYTES, st>>>(a, maps);
     return cudaGetLastError();
 }
 
-template <typename T>
-cudaError_t launch_tm_t(int mode, const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int gc,
+template <typename T, int S>
+cudaError_t launch_tm_s(int mode, const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int gc,
                         cudaStream_t st) {
-    if (mode == MODE_STATES) return launch_tm_one<T, MODE_STATES, false>(a, maps, warps, Bsz, gc, st);
-    return a.z != nullptr ? launch_tm_one<T, MODE_FULL, true>(a, maps, warps, Bsz, gc, st)
-                          : launch_tm_one<T, MODE_FULL, false>(a, maps, warps, Bsz, gc, st);
+    if (mode == MODE_STATES) return launch_tm_one<T, MODE_STATES, false, S>(a, maps, warps, Bsz, gc, st);
+    return a.z != nullptr ? launch_tm_one<T, MODE_FULL, true, S>(a, maps, warps, Bsz, gc, st)
+                          : launch_tm_one<T, MODE_FULL, false, S>(a, maps, warps, Bsz, gc, st);
 }
 
 }  // namespace
@@ -119,17 +120,25 @@ cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &a, long long Bsz
     // TMA coordinates are 32-bit: the time axis and the channel axis must fit
     if (a.L >= (1LL << 31) - 64 || a.Dch >= (1LL << 31) - 128 || Bsz >= (1LL << 31)) return cudaErrorNotSupported;
     const bool bf16 = dtype == 1;
-    const int warps = choose_warps(Bsz, a.Dch, grid_chunks, device_sms());
-    const unsigned ch = 8u * (unsigned)warps;
+    // lanes per channel: each lane owns 4 states; fp32 B/C (three bf16 parts per
+    // value) fit the selector's K = 16 for 4 lanes only
+    const int S = a.N <= 16 ? 4 : a.N <= 32 ? 8 : 16;
+    if (a.N > 64 || (!bf16 && S != 4)) return cudaErrorNotSupported;
+    const int warps = choose_warps(Bsz, a.Dch, grid_chunks, device_sms(), S);
+    const unsigned ch = 32u * (unsigned)warps / (unsigned)S;
     TmMaps maps;
     const bool ok = encode_3d(&maps.u, a.u, bf16, a.L, a.Dch, Bsz, ch, true) &&
                     encode_3d(&maps.delta, a.delta, bf16, a.L, a.Dch, Bsz, ch, true) &&
                     encode_3d(&maps.z, a.z != nullptr ? a.z : a.u, bf16, a.L, a.Dch, Bsz, ch, true) &&
-                    encode_3d(&maps.B, a.Bm, bf16, a.L, a.N, Bsz, 16, false) &&
-                    encode_3d(&maps.C, a.Cm, bf16, a.L, a.N, Bsz, 16, false);
+                    encode_3d(&maps.B, a.Bm, bf16, a.L, a.N, Bsz, 4u * S, false) &&
+                    encode_3d(&maps.C, a.Cm, bf16, a.L, a.N, Bsz, 4u * S, false);
     if (!ok) return cudaErrorNotSupported;
-    return bf16 ? launch_tm_t<bf16_t>(mode, a, maps, warps, Bsz, grid_chunks, st)
-                : launch_tm_t<float>(mode, a, maps, warps, Bsz, grid_chunks, st);
+    if (!bf16) return launch_tm_s<float, 4>(mode, a, maps, warps, Bsz, grid_chunks, st);
+    switch (S) {
+        case 4: return launch_tm_s<bf16_t, 4>(mode, a, maps, warps, Bsz, grid_chunks, st);
+        case 8: return launch_tm_s<bf16_t, 8>(mode, a, maps, warps, Bsz, grid_chunks, st);
+        default: return launch_tm_s<bf16_t, 16>(mode, a, maps, warps, Bsz, grid_chunks, st);
+    }
 }
 
 }  // namespace mamba

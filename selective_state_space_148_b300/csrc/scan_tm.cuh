@@ -26,23 +26,27 @@
 // (h_n(t), h_n(t+1)), which the recurrence writes in place.
 //
 // B and C do not depend on the channel, so all warps of a CTA read the same
-// TMEM columns: a CTA of W warps (8 channels each, 4 lanes per channel, lane
-// m%4 owning states 4(m%4)..+3; warp w reads TMEM lanes 32(w%4)..+31) takes the
-// whole of TMEM (512 columns, one CTA per SM) as two buffers of one 32-step
-// super-tile each.  W (8..12) is chosen per problem so that the CTAs fill the
-// SMs in whole waves.  Per super-tile the CTA does, once: one MMA (M=128,
-// N=256, K=16), five tiled TMA loads (u, Delta_raw, z boxes of 32 steps x 8W
-// channels, B and C boxes of 32 steps x 16 states; out-of-range rows and steps
-// read as zero), one X build and one CTA barrier.  The input ring has 3 stages,
-// loaded two super-tiles ahead; u/Delta_raw/z use the TMA's 16-byte-chunk
-// swizzle so that the 8 channels of a warp hit distinct banks.
+// TMEM columns.  A channel is spread over S = 4, 8 or 16 lanes (N <= 4 S), lane
+// m % S owning states 4(m % S)..+3 (warp w reads TMEM lanes 32(w % 4)..+31, and
+// the selector picks K row m % S, so a lane always receives its own 4 states'
+// B and C: 8 columns per step for every S).  A CTA of W warps (32 W / S
+// channels) takes the whole of TMEM (512 columns, one CTA per SM) as two
+// buffers of one 32-step super-tile each.  W (8..12) is chosen per problem so
+// that the CTAs fill the SMs in whole waves.  Per super-tile the CTA does,
+// once: one MMA (M=128, N=256, K=16), five tiled TMA loads (u, Delta_raw, z
+// boxes of 32 steps x 32 W / S channels, B and C boxes of 32 steps x 4 S
+// states; out-of-range rows and steps read as zero), one X build and one CTA
+// barrier.  The input ring has 3 stages, loaded two super-tiles ahead;
+// u/Delta_raw/z use the TMA's 16-byte-chunk swizzle so that the channels of a
+// warp hit distinct banks.
 //
 // Per 8-step sub-tile i each lane loads its 64 TMEM columns, then in one
 // branch-free block computes Delta = softplus(.), Delta*u, D*u and SiLU(z) for
-// its step pair of sub-tile i+1 (Delta, Delta*u go to shared memory for the
-// channel's 4 lanes; D*u, SiLU(z) stay in registers), finishes y for its pair
-// of sub-tile i-1 (sum of the 4 lanes' C.h partials, + D*u, * SiLU(z),
-// predicated store) and runs the recurrence over sub-tile i's 8 steps.
+// step pair s % 4 of sub-tile i+1 (Delta, Delta*u go to shared memory for the
+// channel's lanes; D*u, SiLU(z) stay in registers), finishes y for that pair
+// of sub-tile i-1 (sum of the channel's S C.h partials, + D*u, * SiLU(z),
+// predicated store by lanes s < 4) and runs the recurrence over sub-tile i's
+// 8 steps.
 //
 // Every mbarrier wait is bounded; a timeout sets a shared abort flag that
 // every later wait honours and that stops further loads and MMAs, is recorded
@@ -69,10 +73,12 @@ struct TmMaps {
     CUtensorMap u, delta, z, B, C;
 };
 
-template <typename T, int MODE>
+// S = lanes per channel (4, 8 or 16: N <= 4 S), each lane owning 4 states.
+template <typename T, int MODE, int S_ = 4>
 struct TmShape {
-    static constexpr int MIN_WARPS = 8, MAX_WARPS = 12;  // CTA width, 8 channels per warp
-    static constexpr int MAX_THR = 32 * MAX_WARPS, MAX_CH = 8 * MAX_WARPS, S = 4;
+    static constexpr int S = S_;
+    static constexpr int MIN_WARPS = 8, MAX_WARPS = 12;  // CTA width, 32 / S channels per warp
+    static constexpr int MAX_THR = 32 * MAX_WARPS, MAX_CH = MAX_THR / S;
     static constexpr int TT = 32;                  // steps per super-tile
     static constexpr int TB = 8;                   // steps per sub-tile
     static constexpr int NSUB = TT / TB;
@@ -82,14 +88,14 @@ struct TmShape {
     static constexpr bool SPLIT = sizeof(T) == 4;
     static constexpr int ROW = TT * (int)sizeof(T);  // bytes of one row of a box
     static constexpr int SWZ = ROW / 16;             // 16-byte chunks per swizzle span (64 B or 128 B)
-    static constexpr int IO_TILE = MAX_CH * ROW;     // slot of one of u, Delta_raw, z (box: 8W rows)
-    static constexpr int BC_TILE = 16 * ROW;         // one of B, C
+    static constexpr int IO_TILE = (MAX_CH * ROW + 1023) / 1024 * 1024;  // slot of u, Delta_raw or z (box: 32 W / S rows)
+    static constexpr int BC_TILE = 4 * S * ROW;      // one of B, C (box: 4 S state rows)
     static constexpr int STAGE_BYTES = 3 * IO_TILE + 2 * BC_TILE;
     static constexpr int A_BYTES = 128 * 16 * 2;
     static constexpr int X_BYTES = COLS * 16 * 2;
-    static constexpr int DU_BYTES = MAX_CH * S * 16;           // per sub-tile: (Delta, Delta', du, du') per lane
-    static constexpr int P_STRIDE = TB + 4;                    // floats per (channel, lane) row of partials
-    static constexpr int P_BYTES = MAX_CH * S * P_STRIDE * 4;  // per sub-tile
+    static constexpr int DU_BYTES = MAX_CH * 4 * 16;           // per sub-tile: (Delta, Delta', du, du') per step pair
+    static constexpr int P_STRIDE = TB + 4;                    // floats per lane row of partials
+    static constexpr int P_BYTES = MAX_THR * P_STRIDE * 4;     // per sub-tile
     static constexpr int OFF_ST = 0;
     static constexpr int OFF_A = OFF_ST + NST * STAGE_BYTES;
     static constexpr int OFF_X = OFF_A + A_BYTES;
@@ -99,14 +105,17 @@ struct TmShape {
     static constexpr int SMEM_BYTES = OFF_BAR + 128 + 1024;  // + room to align the base to 1024 bytes
     static_assert(IO_TILE % 1024 == 0 && BC_TILE % 1024 == 0, "swizzled boxes need 1024-byte aligned tiles");
     static_assert(SWZ == 4 || SWZ == 8, "rows of 64 or 128 bytes");
+    static_assert(S == 4 || S == 8 || S == 16, "4, 8 or 16 lanes per channel");
+    static_assert(!SPLIT || S == 4, "fp32 B/C take 3 K rows per slice: 4 slices fill K = 16");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
-// HAS_Z: the gate z is given (MODE_FULL only).  blockDim.x = 32 W, W in 8..12.
-template <typename T, int MODE, bool HAS_Z>
-__global__ void __launch_bounds__(TmShape<T, MODE>::MAX_THR, 1)
+// HAS_Z: the gate z is given (MODE_FULL only).  S lanes per channel.
+// blockDim.x = 32 W, W in 8..12.
+template <typename T, int MODE, bool HAS_Z, int S_>
+__global__ void __launch_bounds__(TmShape<T, MODE, S_>::MAX_THR, 1)
 scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
-    using Sh = TmShape<T, MODE>;
+    using Sh = TmShape<T, MODE, S_>;
     constexpr bool FAST = sizeof(T) == 2;
     constexpr int S = Sh::S, TT = Sh::TT, TB = Sh::TB, NSUB = Sh::NSUB, COLS = Sh::COLS, MAX_CH = Sh::MAX_CH;
     constexpr int NST = Sh::NST;
@@ -119,8 +128,8 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     unsigned char *const sSt = smem + Sh::OFF_ST;
     uint16_t *const sA = reinterpret_cast<uint16_t *>(smem + Sh::OFF_A);
     unsigned char *const sX = smem + Sh::OFF_X;
-    float4 *const sDU = reinterpret_cast<float4 *>(smem + Sh::OFF_DU);  // [2][MAX_CH][S]
-    float *const sP = reinterpret_cast<float *>(smem + Sh::OFF_P);      // [2][MAX_CH][S][P_STRIDE]
+    float4 *const sDU = reinterpret_cast<float4 *>(smem + Sh::OFF_DU);  // [2][MAX_CH][4 pairs]
+    float *const sP = reinterpret_cast<float *>(smem + Sh::OFF_P);      // [2][MAX_THR][P_STRIDE]
     uint64_t *const full = reinterpret_cast<uint64_t *>(smem + Sh::OFF_BAR);  // [2] MMA of a super-tile done
     uint64_t *const xready = full + 2;                                        // X built by every warp
     uint64_t *const done = full + 3;                                          // abort path: all MMAs done
@@ -128,9 +137,14 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     uint32_t *const taddr_s = reinterpret_cast<uint32_t *>(smem + Sh::OFF_BAR + 64);
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(smem + Sh::OFF_BAR + 68);
 
-    const int nthr = blockDim.x, ch = nthr >> 2;  // channels of this CTA
+    const int nthr = blockDim.x, ch = nthr / S;  // channels of this CTA
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int s = tid & 3, c = tid >> 2;  // channel within the CTA, state slice
+    const int s = tid % S, c = tid / S;  // state slice, channel within the CTA
+    // the 4 step pairs of a sub-tile: lane s handles pair ps for its channel's
+    // Delta and y (lanes s >= 4 of a wider channel repeat lane s % 4's work and
+    // store nothing)
+    const int ps = s & 3;
+    const bool pair_owner = s < 4;
     const long long d0 = (long long)blockIdx.x * ch;
     const long long d = d0 + c;
     const bool valid = d < a.Dch;
@@ -152,7 +166,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     // selector: element (m, k) of the 128 x 16 K-major operand
     for (int i = tid; i < 128 * 16; i += nthr) {
         const int m = i >> 4, kk = i & 15;
-        const bool one = Sh::SPLIT ? (kk < 12 && kk / 3 == (m & 3)) : (kk == (m & 3));
+        const bool one = Sh::SPLIT ? (kk < 12 && kk / 3 == (m & 3)) : (kk == m % S);
         sA[((m >> 3) * 256 + (kk >> 3) * 128 + (m & 7) * 16 + (kk & 7) * 2) >> 1] = one ? 0x3F80u : 0u;
     }
     for (int i = tid; i < 2 * Sh::X_BYTES / 16; i += nthr)
@@ -207,30 +221,41 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         tc::tma_load_3d(st, &maps.u, x, (int)d0, (int)b, bar);
         tc::tma_load_3d(st + Sh::IO_TILE, &maps.delta, x, (int)d0, (int)b, bar);
         if (HAS_Z) tc::tma_load_3d(st + 2 * Sh::IO_TILE, &maps.z, x, (int)d0, (int)b, bar);
-        tc::tma_load_3d(st + 3 * Sh::IO_TILE, &maps.B, x, 0, (int)b, bar);
+        tc::tma_load_3d(st + 3 * Sh::IO_TILE, &maps.B, x, 0, (int)b, bar);  // 4 S state rows, zero past N
         tc::tma_load_3d(st + 3 * Sh::IO_TILE + Sh::BC_TILE, &maps.C, x, 0, (int)b, bar);
     };
     int last_loaded = -1;  // thread 0: latest super-tile whose loads were issued
 
-    // X of one super-tile from its stage: column n = 16 * pair + j (column order above)
+    // X of one super-tile from its stage: column n = 16 * pair + j (column order
+    // above), K row k = slice k's value (bf16), or K rows 3k..3k+2 its three
+    // bf16 parts (fp32, S = 4)
     auto x_build = [&](int xb, const unsigned char *st) {
-        const T *raw = reinterpret_cast<const T *>(st + 3 * Sh::IO_TILE);  // [which][16][TT]
+        const T *raw = reinterpret_cast<const T *>(st + 3 * Sh::IO_TILE);  // [which][4 S][TT]
         unsigned char *xbase = sX + xb * Sh::X_BYTES;
         for (int n = tid; n < COLS; n += nthr) {
             const int j = n & 15;
             const int t = 2 * (n >> 4) + (j & 1);
             const int which = j >> 3, col = (j & 7) >> 1;
-            float v[4];
+            float v[S];
 #pragma unroll
-            for (int sl = 0; sl < 4; ++sl) {
-                const T *p = raw + (which * 16 + 4 * sl + col) * TT + t;
+            for (int sl = 0; sl < S; ++sl) {
+                const T *p = raw + (which * 4 * S + 4 * sl + col) * TT + t;
                 v[sl] = Sh::SPLIT ? *reinterpret_cast<const float *>(p)
                                   : __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t *>(p)) << 16);
             }
             unsigned char *dst = xbase + (n >> 3) * 256 + (n & 7) * 16;
-            if (!Sh::SPLIT) {
-                // bf16 inputs are exact in bf16: K rows 0..3
-                *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+            if constexpr (!Sh::SPLIT) {
+                // bf16 inputs are exact in bf16; K rows 0..7 at dst, 8..15 at dst + 128
+                uint32_t w[S / 2];
+#pragma unroll
+                for (int k = 0; k < S / 2; ++k) w[k] = pack_bf16x2(v[2 * k], v[2 * k + 1]);
+                if constexpr (S == 4) {
+                    *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+                } else {
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+                    if constexpr (S == 16)
+                        *reinterpret_cast<uint4 *>(dst + 128) = make_uint4(w[4], w[5], w[6], w[7]);
+                }
             } else {
                 // fp32: value = hi + mid + lo, three bf16 parts, K rows 3*sl .. 3*sl+2
                 uint32_t hb[12];
@@ -262,13 +287,13 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     int sw_off[NSUB];  // swizzled byte offset of this lane's pair in sub-tile q
 #pragma unroll
     for (int q = 0; q < NSUB; ++q) {
-        const int o = c * Sh::ROW + (q * TB + 2 * s) * (int)sizeof(T);
+        const int o = c * Sh::ROW + (q * TB + 2 * ps) * (int)sizeof(T);
         sw_off[q] = o ^ (((o >> 7) & (Sh::SWZ - 1)) << 4);
     }
     auto stage_word = [&](const unsigned char *st, int tensor, int q) -> Word {
         return *reinterpret_cast<const Word *>(st + tensor * Sh::IO_TILE + sw_off[q]);
     };
-    float4 *const du_mine = sDU + c * S + s;  // + (i & 1) * MAX_CH * S
+    float4 *const du_chan = sDU + c * 4;  // + (i & 1) * MAX_CH * 4 + pair
     // Delta, Delta * u of this lane's pair at offset r (sub-tile parity par) ->
     // sDU; D * u and SiLU(z) stay in this lane's registers until y of the pair is formed
     float sdt_acc = 0.f;  // MODE_STATES: this lane's share of sum(Delta) over the chunk
@@ -279,24 +304,24 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         float2 dl = softplus ? softplus2<FAST>(raw) : raw;
         dl = in ? dl : f2(0.f, 0.f);
         const float2 du = __fmul2_rn(dl, u);  // zero outside the range: u there is finite box fill or data
-        du_mine[par * MAX_CH * S] = make_float4(dl.x, dl.y, du.x, du.y);
-        if (MODE == MODE_STATES) sdt_acc += dl.x + dl.y;
+        if (pair_owner) du_chan[par * MAX_CH * 4 + ps] = make_float4(dl.x, dl.y, du.x, du.y);
+        if (MODE == MODE_STATES && pair_owner) sdt_acc += dl.x + dl.y;
         if (MODE == MODE_FULL) {
             Du = __fmul2_rn(D2, u);
             if (HAS_Z) g = silu2<FAST>(unpack(stage_word(st, 2, q)));
         }
     };
-    const float *const p_mine = sP + (c * S) * Sh::P_STRIDE + 2 * s;  // + (i & 1) * MAX_CH * S * P_STRIDE
+    const float *const p_chan = sP + (c * S) * Sh::P_STRIDE + 2 * ps;  // + (i & 1) * MAX_THR * P_STRIDE
     // y of this lane's pair at offset r from the channel's 4 partial sums
     auto output_pair = [&](int r, int par, float2 Du, float2 g) {
         if (MODE != MODE_FULL) return;
-        const float *pp = p_mine + par * MAX_CH * S * Sh::P_STRIDE;
+        const float *pp = p_chan + par * Sh::MAX_THR * Sh::P_STRIDE;
         float2 ys = *reinterpret_cast<const float2 *>(pp);
 #pragma unroll
         for (int k = 1; k < S; ++k) ys = __fadd2_rn(ys, *reinterpret_cast<const float2 *>(pp + k * Sh::P_STRIDE));
         float2 yy = __fadd2_rn(ys, Du);
         if (HAS_Z) yy = __fmul2_rn(yy, g);
-        const bool st = (unsigned)r < lenv;
+        const bool st = pair_owner && (unsigned)r < lenv;
         if constexpr (Sh::SPLIT)
             st_f32x2_if(ylane + r, yy, st);
         else
@@ -335,7 +360,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     }
     // (D u, SiLU z) of the step pairs whose y is still open, by sub-tile parity
     float2 Du_r[2], g_r[2];
-    side_pair(stage_of(0), 0, 2 * s, 0, Du_r[0], g_r[0]);
+    side_pair(stage_of(0), 0, 2 * ps, 0, Du_r[0], g_r[0]);
     __syncwarp();
 
     int k_cur = 0;  // stage of super-tile sup
@@ -372,7 +397,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         tc::fence_after_sync();
         const unsigned char *st_cur = stage_of(k_cur);
         const unsigned char *st_nxt = stage_of(k_nxt);
-        const int r0 = sup * TT + 2 * s;  // this lane's pair offset in sub-tile 0 of this super-tile
+        const int r0 = sup * TT + 2 * ps;  // this lane's pair offset in sub-tile 0 of this super-tile
 #pragma unroll
         for (int q = 0; q < NSUB; ++q) {
             uint32_t bcu[2][32];
@@ -384,7 +409,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
             // recurrence of sub-tile i (i = 4 sup + q, so i & 1 == q & 1)
             float4 dq[TB / 2];
 #pragma unroll
-            for (int p = 0; p < TB / 2; ++p) dq[p] = du_mine[(q & 1) * MAX_CH * S - s + p];
+            for (int p = 0; p < TB / 2; ++p) dq[p] = du_chan[(q & 1) * MAX_CH * 4 + p];
             output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
             if (q + 1 < NSUB)
                 side_pair(st_cur, q + 1, r0 + (q + 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
@@ -413,7 +438,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                 }
             }
             if (MODE == MODE_FULL) {
-                float *prow = const_cast<float *>(p_mine) - 2 * s + s * Sh::P_STRIDE + (q & 1) * MAX_CH * S * Sh::P_STRIDE;
+                float *prow = sP + ((q & 1) * Sh::MAX_THR + tid) * Sh::P_STRIDE;
                 *reinterpret_cast<float4 *>(prow) = make_float4(pq[0], pq[1], pq[2], pq[3]);
                 *reinterpret_cast<float4 *>(prow + 4) = make_float4(pq[4], pq[5], pq[6], pq[7]);
             }
@@ -422,7 +447,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         k_cur = k_nxt;
     }
 
-    output_pair((nsup - 1) * TT + 3 * TB + 2 * s, 1, Du_r[1], g_r[1]);  // the last sub-tile is odd
+    output_pair((nsup - 1) * TT + 3 * TB + 2 * ps, 1, Du_r[1], g_r[1]);  // the last sub-tile is odd
     if (MODE == MODE_STATES) {
         float sdt = sdt_acc;
 #pragma unroll

@@ -310,3 +310,19 @@ def test_flags_unaligned_and_ragged():
     yr, hr = run_oracle(x, disc=1, reverse=True)
     assert_close(to_host_f64(y), yr, TOL_Y["bf16"], "flags unaligned y")
     assert_close(last.cpu().numpy().astype(np.float64), hr, TOL_STATE, "flags unaligned last_state")
+
+
+# ----------------------------------------------------------------------------- tensor-memory kernel, N up to 64
+
+@pytest.mark.parametrize("N", [9, 12, 16, 17, 20, 32, 33, 40, 64])
+@pytest.mark.parametrize("L", [72, 256])
+def test_aligned_state_sizes(N, L):
+    """16-byte aligned rows (the tensor-memory kernel for bf16, 8 < N <= 64): direct, no gate, and chunked with h0."""
+    x = inputs.make_scan_inputs(2, 45, N, L, io="bf16", seed=50 + N)
+    check(x, f"aligned N={N} L={L}")
+    check(x, f"aligned N={N} L={L} no z", with_z=False)
+    h0 = np.random.default_rng(N).normal(0, 0.3, (2, 45, N)).astype(np.float32)
+    yg, hg = run_gpu(x, h0=h0, chunk_len=64)
+    yr, hr = run_oracle(x, h0=h0.astype(np.float64))
+    assert_close(yg, yr, TOL_Y["bf16"], f"aligned chunked N={N} L={L} y")
+    assert_close(hg, hr, TOL_STATE, f"aligned chunked N={N} L={L} last_state")
