@@ -238,7 +238,7 @@ int mamba_state_update(float *state, const void *u, const void *delta, const flo
     a.Dch = Dch;
     a.N = N;
     a.softplus = softplus_flag ? 1 : 0;
-    const bool vec = (N % 4 == 0) && aligned16(state) && aligned16(A);
+    const bool vec = (N % 4 == 0) && aligned16(state) && aligned16(A) && Bsz * Dch < (1LL << 31);
     return launch_state_update(dtype, vec, a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? MAMBA_OK
                : MAMBA_ERR_LAUNCH;
