@@ -50,6 +50,8 @@ def _load():
                                               i64, i64, i64, i64]
         lib.oracle_state_update.restype = None
         lib.oracle_state_update.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, ci, ci, dp, i64, i64, i64]
+        lib.oracle_causal_conv1d.restype = None
+        lib.oracle_causal_conv1d.argtypes = [dp, dp, dp, ci, dp, i64, i64, i64, i64]
         lib.oracle_num_threads.restype = ci
         lib.oracle_set_num_threads.argtypes = [ci]
         _lib = lib
@@ -125,3 +127,19 @@ def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, soft
                                 _ptr(z), _ptr(delta_bias), int(bool(softplus_flag)), int(disc), _ptr(y),
                                 Bsz, Dch, N)
     return y, st
+
+
+def causal_conv1d(x, w, bias=None, silu=True):
+    """Depthwise causal convolution (width W = w.shape[1]) of x [Bsz, Dch, L], then SiLU.
+
+    pre_t = bias_d + sum_k w[d, k] x_{t-(W-1)+k} with x_s = 0 for s < 0 (the pages' Conv1d with
+    groups = d_inner, padding = W - 1, first L outputs), u = SiLU(pre) when silu is true.
+    """
+    x = _f64(x)
+    Bsz, Dch, L = x.shape
+    w = _f64(w)
+    assert w.shape[0] == Dch
+    b = None if bias is None else _f64(bias)
+    u = np.empty_like(x)
+    _load().oracle_causal_conv1d(_ptr(x), _ptr(w), _ptr(b), int(bool(silu)), _ptr(u), Bsz * Dch, Dch, L, w.shape[1])
+    return u

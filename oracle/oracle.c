@@ -18,7 +18,9 @@
  *         §4.1 / §4.2 step 5 (output multiplied by the gate branch).
  *   [XW]  "Mamba: Linear-Time Sequence Modeling with Selective State Spaces"
  *         summary (ai.xwebgame.com), "running it in PyTorch" block: the gate
- *         is SiLU of the residual branch.
+ *         is SiLU of the residual branch; the branch that feeds the scan is a
+ *         depthwise causal Conv1d (kernel 4, padding 3, first L outputs)
+ *         followed by SiLU.
  *
  * Readings where the pages are silent (each one is listed in the design
  * notes): y_t reads the state *after* the update with token t; D*u is added
@@ -156,6 +158,36 @@ void oracle_state_update(double *state, const double *u, const double *dt_raw,
 }
 
 /* Number of host threads the parallel loops above will use. */
+/*
+ * Depthwise causal convolution of width W followed by SiLU, per row
+ * r = b * Dch + d of x [nrows][L]:
+ *   pre_t = bias_d + sum_{k=0}^{W-1} w[d][k] * x_{t-(W-1)+k}   (x_s = 0 for s < 0)
+ *   u_t   = silu_flag ? pre_t / (1 + exp(-pre_t)) : pre_t
+ * [XW] "running it in PyTorch" block: nn.Conv1d(d_inner, d_inner,
+ * kernel_size=d_conv (4), groups=d_inner, padding=d_conv-1), keep the first L
+ * outputs, then nn.SiLU -- the branch that feeds the selective scan ([FS] §4:
+ * causal convolution before the scan).  bias may be NULL (0).
+ */
+void oracle_causal_conv1d(const double *x, const double *w, const double *bias,
+                          int silu_flag, double *u, int64_t nrows, int64_t Dch,
+                          int64_t L, int64_t W) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t d = r % Dch;
+        const double *xr = x + r * L;
+        for (int64_t t = 0; t < L; ++t) {
+            double pre = bias ? bias[d] : 0.0;
+            for (int64_t k = 0; k < W; ++k) {
+                const int64_t s = t - (W - 1) + k;
+                if (s >= 0) pre += w[d * W + k] * xr[s];
+            }
+            u[r * L + t] = silu_flag ? silu(pre) : pre;
+        }
+    }
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();

@@ -334,3 +334,72 @@ def test_channels_independent_and_broadcast():
                                            c["z"][b:b + 1, d:d + 1], c["delta_bias"][d:d + 1])
             np.testing.assert_array_equal(y1[0, 0], y[b, d])
             np.testing.assert_array_equal(h1[0, 0], h[b, d])
+
+
+# ----------------------------------------------------------------------------- causal conv1d + SiLU (the branch feeding the scan)
+# ai.xwebgame.com summary, "running it in PyTorch" block: Conv1d(d_inner, d_inner, kernel_size=4,
+# groups=d_inner, padding=3), first L outputs, then SiLU.
+
+def _conv_case(seed, Bsz=2, Dch=5, L=23, W=4):
+    r = np.random.default_rng(seed)
+    return r.normal(size=(Bsz, Dch, L)), r.normal(size=(Dch, W)), r.normal(size=Dch)
+
+
+def test_conv_identity_tap_is_the_input():
+    x, w, _ = _conv_case(0)
+    w[:] = 0.0
+    w[:, 3] = 1.0                      # the tap on x_t itself
+    assert np.array_equal(oracle.causal_conv1d(x, w, None, silu=False), x)
+
+
+def test_conv_shift_tap_delays_by_one_with_zero_padding():
+    x, w, _ = _conv_case(1)
+    w[:] = 0.0
+    w[:, 2] = 1.0                      # the tap on x_{t-1}
+    u = oracle.causal_conv1d(x, w, None, silu=False)
+    assert np.array_equal(u[..., 1:], x[..., :-1])
+    assert np.all(u[..., 0] == 0.0)
+
+
+def test_conv_matches_numpy_convolution():
+    """pre_t = b + sum_k w_k x_{t-3+k} is the first L terms of the full convolution with the reversed taps."""
+    x, w, b = _conv_case(2)
+    u = oracle.causal_conv1d(x, w, b, silu=False)
+    ref = np.stack([[np.convolve(x[i, d], w[d][::-1])[:x.shape[2]] + b[d] for d in range(x.shape[1])]
+                    for i in range(x.shape[0])])
+    np.testing.assert_allclose(u, ref, rtol=0, atol=1e-13)
+
+
+def test_conv_is_causal_with_a_width_four_window():
+    x, w, b = _conv_case(3)
+    u0 = oracle.causal_conv1d(x, w, b)
+    x2 = x.copy()
+    x2[1, 2, 10] += 1.0
+    u1 = oracle.causal_conv1d(x2, w, b)
+    changed = np.argwhere(u1 != u0)
+    assert {tuple(c) for c in changed} == {(1, 2, t) for t in range(10, 14)}
+
+
+def test_conv_silu_values():
+    """SiLU(0) = 0, SiLU(1) = 1/(1+e^-1) = 0.7310585786300049, SiLU(-1) = -0.2689414213699951."""
+    x = np.array([[[0.0, 1.0, -1.0]]])
+    w = np.array([[0.0, 0.0, 0.0, 1.0]])
+    u = oracle.causal_conv1d(x, w, None, silu=True)
+    np.testing.assert_allclose(u[0, 0], [0.0, 0.7310585786300049, -0.2689414213699951], rtol=0, atol=1e-15)
+
+
+def test_conv_then_scan_composes_with_the_scan_oracle():
+    """The fused path's reference is the scan of u = SiLU(conv(x)): with the identity tap and no bias
+    it reduces to the scan of SiLU(x)."""
+    r = np.random.default_rng(4)
+    Bsz, Dch, L, N = 1, 3, 17, 4
+    x = r.normal(size=(Bsz, Dch, L))
+    w = np.zeros((Dch, 4))
+    w[:, 3] = 1.0
+    delta, A = r.normal(size=(Bsz, Dch, L)) - 2, -np.tile(np.arange(1.0, N + 1), (Dch, 1))
+    B, C = r.normal(size=(Bsz, N, L)), r.normal(size=(Bsz, N, L))
+    u = oracle.causal_conv1d(x, w, None)
+    y1, h1 = oracle.selective_scan(u, delta, A, B, C)
+    y2, h2 = oracle.selective_scan(x / (1 + np.exp(-x)), delta, A, B, C)
+    np.testing.assert_allclose(y1, y2, rtol=1e-13, atol=1e-13)
+    np.testing.assert_allclose(h1, h2, rtol=1e-13, atol=1e-13)
