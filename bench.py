@@ -221,6 +221,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--conv", default="none", choices=["none", "fused", "two-step"],
+                    help="feed the scan through the depthwise causal conv1d + SiLU branch: fused into the scan "
+                         "kernel, or as a separate convolution launch before the scan")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -255,7 +258,7 @@ def main():
     peaks = measured_peaks()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not decode:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not decode and args.conv == "none":
         bps, ups, info = time_oracle(res["inputs"])
         cpu = {"value": bps / 1e9, "unit": "GB/s", "cores": info["threads"], "kind": "oracle",
                "sample": f"float64 oracle over whole time rows of {info['channels']} of {info['of']} channels "
@@ -346,11 +349,22 @@ def bench_scan(args, m, torch):
     ws_bytes = m.mamba_scan_workspace_size(Bsz, Dch, L, N, 0, m.MAMBA_BF16 if io == "bf16" else m.MAMBA_F32)
     chunked = ws_bytes > 0
     stream = torch.cuda.current_stream()
+    if args.conv != "none":   # s["u"] then holds x, the convolution's input
+        cw, cb = (torch.from_numpy(a).to(dev) for a in inputs.conv_params(Dch, 7))
+        u_tmp = torch.empty_like(base["u"])
+
+    def run(s, y, h):
+        if args.conv == "fused":
+            m.mamba_selective_scan_fwd_conv(s["u"], cw, cb, s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h,
+                                            stream=stream)
+        elif args.conv == "two-step":
+            m.mamba_causal_conv1d_silu(s["u"], cw, cb, 1, u_tmp, stream=stream)
+            m.mamba_selective_scan_fwd(u_tmp, s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h, stream=stream)
+        else:
+            m.mamba_selective_scan_fwd(s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h, stream=stream)
 
     def step(i):
-        s = sets[i % R]
-        m.mamba_selective_scan_fwd(s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, ys[i % R], hs[i % R],
-                                   stream=stream)
+        run(sets[i % R], ys[i % R], hs[i % R])
 
     mufu_per_clk, sms = mufu_ex2_per_clk_per_sm(m, torch)
     for i in range(args.warmup):
@@ -376,8 +390,7 @@ def bench_scan(args, m, torch):
     def e2e_step(i):
         for k in dsets:
             dsets[k].copy_(hsrc[k], non_blocking=True)
-        m.mamba_selective_scan_fwd(dsets["u"], dsets["delta"], A, dsets["B"], dsets["C"], D, dsets["z"], bias, 1,
-                                   ys[0], hs[0], stream=stream)
+        run(dsets, ys[0], hs[0])
         hy.copy_(ys[0], non_blocking=True)
         hh.copy_(hs[0], non_blocking=True)
 
@@ -401,8 +414,10 @@ def bench_scan(args, m, torch):
     mufu_peak = SM_COUNT_NOMINAL * mufu_units * peaks["sm_max_mhz"] * 1e6   # ex2 per second
     t_mufu = exps / mufu_peak
     t_meas = t_ms * 1e-3
-    tm = 8 < N <= 16 and os.environ.get("MAMBA_SCAN_KERNEL") != "smem"
-    kernel = (f"scan_tm_kernel<{io},full,z>" if tm else f"scan_kernel<{io},NP{1 << max(2, (N - 1).bit_length())},full>")
+    tm = 8 < N <= 64 and (io == "bf16" or N <= 16) and os.environ.get("MAMBA_SCAN_KERNEL") != "smem"
+    kernel = (f"scan_tm_kernel<{io},full,z,S{4 if N <= 16 else 8 if N <= 32 else 16}"
+              f"{',conv' if args.conv == 'fused' else ''}>" if tm
+              else f"scan_kernel<{io},NP{1 << max(2, (N - 1).bit_length())},full>")
     traffic = traffic_record(f"{args.workload}")
     if t_mufu >= t_hbm:
         roof = {"bound": "alu", "achieved": round(exps / t_meas / 1e12, 4),
@@ -418,12 +433,18 @@ def bench_scan(args, m, torch):
                 "peak_source": f"{peaks['source']} copy bandwidth"}
     if chunked:
         roof["note"] = "chunked scan: the step is three launches (chunk states, carry, rescan); figures are per step"
+    if args.conv == "two-step":
+        roof["note"] = (roof.get("note", "") + "; " if "note" in roof else "") + \
+            "two launches per step (convolution, then scan); figures are per step"
     return dict(ms_per_step=t_ms, bytes=nbytes, tokens=Bsz * L, dtype="f32" if io == "f32" else "bf16",
                 config={"workload": args.workload, "batch": Bsz, "d_inner": Dch, "d_state": N, "seq_len": L,
                         "io": io, "state": "fp32", "l2": f"inputs rotate over {R} resident copies "
                                                           f"({R * nbytes / 1e6:.0f} MB > L2)",
-                        "path": "chunked" if chunked else "direct"},
-                roofline=roof, h2d=h2d, d2h=d2h, e2e_ms=e2e_ms, launches=args.steps * (3 if chunked else 1),
+                        "path": "chunked" if chunked else "direct",
+                        **({"conv": args.conv + " (depthwise causal conv1d k=4 + SiLU feeding u)"}
+                           if args.conv != "none" else {})},
+                roofline=roof, h2d=h2d, d2h=d2h, e2e_ms=e2e_ms,
+                launches=args.steps * ((3 if chunked else 1) + (1 if args.conv == "two-step" else 0)),
                 clocks=clocks, inputs=x,
                 mufu={"ex2_per_clk_per_sm": round(mufu_per_clk, 3), "sms": sms})
 

@@ -154,6 +154,41 @@ int mamba_state_update(float *state, const void *u, const void *delta, const flo
                        int64_t Dch, int64_t N, int dtype, mamba_stream_t stream);
 
 /*
+ * Depthwise causal convolution of width 4 followed by SiLU -- the branch that
+ * turns x into the scan's input u (ai.xwebgame.com summary, "running it in
+ * PyTorch" block: Conv1d(d_inner, d_inner, kernel_size=4, groups=d_inner,
+ * padding=3), first L outputs, then SiLU):
+ *   u[b][d][t] = SiLU(conv_bias[d] + sum_{k=0..3} conv_w[d][k] x[b][d][t-3+k]),
+ *   x[b][d][s] = 0 for s < 0.
+ *
+ *   x, u        [Bsz][Dch][L], dtype MAMBA_BF16 or MAMBA_F32 (u may not alias x)
+ *   conv_w      [Dch][4] fp32;  conv_bias [Dch] fp32 or NULL (0)
+ *   silu_flag   non-zero: apply SiLU; zero: write the convolution itself
+ * Caller-owned device memory; nothing is allocated or retained.  Returns
+ * MAMBA_OK, MAMBA_ERR_NULL_ARG, MAMBA_ERR_BAD_SHAPE, MAMBA_ERR_BAD_DTYPE or
+ * MAMBA_ERR_LAUNCH.
+ */
+int mamba_causal_conv1d_silu(const void *x, const float *conv_w, const float *conv_bias, int silu_flag, void *u,
+                             int64_t Bsz, int64_t Dch, int64_t L, int dtype, mamba_stream_t stream);
+
+/*
+ * Selective scan fed by the convolution branch: the scan of
+ * mamba_selective_scan_fwd with u = SiLU(causal_conv1d(x)) (the function
+ * above), u formed inside the scan kernel from x without a round trip through
+ * memory where the tensor-memory kernel runs (bf16, 8 < N <= 16, 16-byte
+ * aligned rows, gate given); other cases run the convolution into a
+ * stream-ordered temporary and then the scan.  y, last_state, D, z, delta_bias
+ * as in mamba_selective_scan_fwd; the D * u term of y uses the convolved u.
+ * conv_w [Dch][4] fp32, conv_bias [Dch] fp32 or NULL; x [Bsz][Dch][L] in place
+ * of u.  Returns the statuses of mamba_selective_scan_fwd.
+ */
+int mamba_selective_scan_fwd_conv(const void *x, const float *conv_w, const float *conv_bias, const void *delta,
+                                  const float *A, const void *B, const void *C, const float *D, const void *z,
+                                  const float *delta_bias, int softplus_flag, void *y, float *last_state,
+                                  int64_t Bsz, int64_t Dch, int64_t L, int64_t N, int dtype,
+                                  mamba_stream_t stream);
+
+/*
  * Chunked forward scan that allocates no device memory (no counterpart in the
  * pages: this is a deployment variant of the chunked scan above).
  *

@@ -62,6 +62,11 @@ def lib() -> ctypes.CDLL:
         L.mamba_status_string.argtypes = [ci]
         L.mamba_device_error.restype = ci
         L.mamba_device_error.argtypes = []
+        L.mamba_causal_conv1d_silu.restype = ci
+        L.mamba_causal_conv1d_silu.argtypes = [vp, vp, vp, ci, vp, i64, i64, i64, ci, vp]
+        L.mamba_selective_scan_fwd_conv.restype = ci
+        L.mamba_selective_scan_fwd_conv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, vp, vp, i64, i64,
+                                                    i64, i64, ci, vp]
         L.mamba_bench_ex2.restype = ci
         L.mamba_bench_ex2.argtypes = [vp, vp, i64, ci, ci, vp]
         _lib = L
@@ -137,6 +142,27 @@ def mamba_selective_scan_fwd_noalloc(u, delta, A, B, C, D, z, delta_bias, softpl
                                                 _ptr(h0), Bsz, Dch, L, N, _dtype_code(u), int(chunk_len),
                                                 _stream(stream))
     _check(st, "mamba_selective_scan_fwd_noalloc")
+
+
+def mamba_causal_conv1d_silu(x, conv_w, conv_bias, silu_flag, u, stream=None):
+    """u = SiLU(conv_bias + depthwise causal width-4 convolution of x).  x, u [Bsz, Dch, L];
+    conv_w [Dch, 4] fp32; conv_bias [Dch] fp32 or None."""
+    Bsz, Dch, L = x.shape
+    st = lib().mamba_causal_conv1d_silu(_ptr(x), _ptr(conv_w), _ptr(conv_bias), int(bool(silu_flag)), _ptr(u),
+                                        Bsz, Dch, L, _dtype_code(x), _stream(stream))
+    _check(st, "mamba_causal_conv1d_silu")
+
+
+def mamba_selective_scan_fwd_conv(x, conv_w, conv_bias, delta, A, B, C, D, z, delta_bias, softplus_flag, y,
+                                  last_state, stream=None):
+    """Selective scan of u = SiLU(causal conv(x)) (the convolution branch fused into the scan)."""
+    Bsz, Dch, L = x.shape
+    N = A.shape[1]
+    st = lib().mamba_selective_scan_fwd_conv(_ptr(x), _ptr(conv_w), _ptr(conv_bias), _ptr(delta), _ptr(A), _ptr(B),
+                                             _ptr(C), _ptr(D), _ptr(z), _ptr(delta_bias), int(bool(softplus_flag)),
+                                             _ptr(y), _ptr(last_state), Bsz, Dch, L, N, _dtype_code(x),
+                                             _stream(stream))
+    _check(st, "mamba_selective_scan_fwd_conv")
 
 
 def mamba_scan_workspace_size(Bsz, Dch, L, N, chunk_len=0, dtype=MAMBA_BF16) -> int:

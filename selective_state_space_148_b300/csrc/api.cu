@@ -26,6 +26,10 @@ bool inject_alloc_failure() {
     return v != nullptr && std::strcmp(v, "alloc") == 0;
 }
 
+bool u_ok_args(const void *delta, const float *A, const void *B, const void *C, const void *y) {
+    return delta && A && B && C && y;
+}
+
 int sm_count(int *out) {
     static int cache[kMaxDevices] = {};
     int dev = 0;
@@ -110,10 +114,15 @@ size_t workspace_bytes_for(long long Bsz, long long Dch, long long N, int K) {
     return h + s;
 }
 
+// Internal status of scan_impl with conv taps: the convolution-fed kernel
+// declined the problem before anything was launched (the caller falls back).
+constexpr int kNotFused = 1;
+
 int scan_impl(const void *u, const void *delta, const float *A, const void *B, const void *C, const float *D,
               const void *z, const float *delta_bias, int softplus_flag, void *y, float *last_state,
               const float *h0, long long Bsz, long long Dch, long long L, long long N, int dtype, int flags,
-              long long chunk_len, void *workspace, size_t workspace_bytes, cudaStream_t stream) {
+              long long chunk_len, void *workspace, size_t workspace_bytes, cudaStream_t stream,
+              const float *conv_w = nullptr, const float *conv_b = nullptr) {
     if (!u || !delta || !A || !B || !C || !y) return MAMBA_ERR_NULL_ARG;
     int st = check_sizes(Bsz, Dch, L, N, dtype);
     if (st != MAMBA_OK) return st;
@@ -142,12 +151,16 @@ int scan_impl(const void *u, const void *delta, const float *A, const void *B, c
     a.N = N;
     a.softplus = softplus_flag ? 1 : 0;
     a.flags = flags;
+    a.conv_w = conv_w;
+    a.conv_b = conv_b;
 
     if (plan.K == 1) {
         a.hin = h0;
         a.chunk_len = L;
         a.nchunks = 1;
-        return launch_scan(dtype, MODE_FULL, vec, a, Bsz, 1, stream) == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+        const cudaError_t e = launch_scan(dtype, MODE_FULL, vec, a, Bsz, 1, stream);
+        if (e == cudaErrorNotSupported && conv_w != nullptr) return kNotFused;
+        return e == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
     }
 
     // chunked scan: pass A (chunk end states), carry, pass B (seeded rescan)
@@ -174,7 +187,12 @@ int scan_impl(const void *u, const void *delta, const float *A, const void *B, c
     a.hin = nullptr;
     a.ws_h = ws_h;
     a.ws_sdt = ws_sdt;
-    if (launch_scan(dtype, MODE_STATES, vec, a, Bsz, plan.K - 1, stream) != cudaSuccess) rc = MAMBA_ERR_LAUNCH;
+    const cudaError_t ea = launch_scan(dtype, MODE_STATES, vec, a, Bsz, plan.K - 1, stream);
+    if (ea == cudaErrorNotSupported && conv_w != nullptr) {  // nothing launched yet
+        if (owned) cudaFreeAsync(ws, stream);
+        return kNotFused;
+    }
+    if (ea != cudaSuccess) rc = MAMBA_ERR_LAUNCH;
     if (rc == MAMBA_OK && launch_carry(A, h0, ws_h, ws_sdt, Bsz, Dch, N, plan.K, stream) != cudaSuccess)
         rc = MAMBA_ERR_LAUNCH;
     a.hin = ws_h;
@@ -260,6 +278,53 @@ const char *mamba_status_string(int status) {
         case MAMBA_ERR_SCRATCH_LIMIT: return "problem needs more scratch than the no-allocation entry point holds";
         default: return "unknown status";
     }
+}
+
+int mamba_causal_conv1d_silu(const void *x, const float *conv_w, const float *conv_bias, int silu_flag, void *u,
+                             int64_t Bsz, int64_t Dch, int64_t L, int dtype, mamba_stream_t stream) {
+    if (!x || !conv_w || !u) return MAMBA_ERR_NULL_ARG;
+    if (dtype != MAMBA_F32 && dtype != MAMBA_BF16) return MAMBA_ERR_BAD_DTYPE;
+    if (Bsz <= 0 || Dch <= 0 || L <= 0 || Bsz > kMaxDim || Dch > kMaxDim || L > kMaxDim || Bsz * Dch > kMaxDim / L)
+        return MAMBA_ERR_BAD_SHAPE;
+    const bool vec = aligned16(x) && aligned16(u) && aligned16(conv_w) && (L * io_bytes(dtype)) % 16 == 0;
+    return launch_conv1d(dtype, vec, x, conv_w, conv_bias, silu_flag ? 1 : 0, u, Bsz * Dch, Dch, L,
+                         reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? MAMBA_OK
+               : MAMBA_ERR_LAUNCH;
+}
+
+int mamba_selective_scan_fwd_conv(const void *x, const float *conv_w, const float *conv_bias, const void *delta,
+                                  const float *A, const void *B, const void *C, const float *D, const void *z,
+                                  const float *delta_bias, int softplus_flag, void *y, float *last_state,
+                                  int64_t Bsz, int64_t Dch, int64_t L, int64_t N, int dtype,
+                                  mamba_stream_t stream) {
+    if (!x || !conv_w) return MAMBA_ERR_NULL_ARG;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (z != nullptr) {  // the fused kernel is built with the gate
+        const int rc = scan_impl(x, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, nullptr, Bsz,
+                                 Dch, L, N, dtype, 0, 0, nullptr, 0, st, conv_w, conv_bias);
+        if (rc != kNotFused) return rc;
+    } else {
+        const int chk = check_sizes(Bsz, Dch, L, N, dtype);
+        if (chk != MAMBA_OK) return chk;
+        if (!u_ok_args(delta, A, B, C, y)) return MAMBA_ERR_NULL_ARG;
+    }
+    // two steps: the convolution into a stream-ordered temporary, then the scan
+    void *u = nullptr;
+    if (inject_alloc_failure()) return MAMBA_ERR_ALLOC;
+    if (cudaMallocAsync(&u, (size_t)(Bsz * Dch * L) * io_bytes(dtype), st) != cudaSuccess) {
+        cudaGetLastError();
+        return MAMBA_ERR_ALLOC;
+    }
+    int rc = mamba_causal_conv1d_silu(x, conv_w, conv_bias, 1, u, Bsz, Dch, L, dtype, stream);
+    if (rc == MAMBA_OK)
+        rc = scan_impl(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, nullptr, Bsz, Dch, L, N,
+                       dtype, 0, 0, nullptr, 0, st);
+    if (cudaFreeAsync(u, st) != cudaSuccess) {
+        cudaGetLastError();
+        if (rc == MAMBA_OK) rc = MAMBA_ERR_LAUNCH;
+    }
+    return rc;
 }
 
 int mamba_bench_ex2(int64_t *cycles, float *sink, int64_t iters, int blocks, int threads, mamba_stream_t stream) {

@@ -47,6 +47,11 @@ struct StepArgs {
 };
 cudaError_t launch_state_update(int dtype, bool vec, const StepArgs &a, cudaStream_t st);
 
+// Depthwise causal conv (width 4) + optional SiLU over rows of length L
+// (row r uses taps w[r % Dch]); vec: 16-byte aligned x, u, w and 16-byte rows.
+cudaError_t launch_conv1d(int dtype, bool vec, const void *x, const float *w, const float *bias, int silu, void *u,
+                          long long rows, long long Dch, long long L, cudaStream_t st);
+
 cudaError_t launch_bench_ex2(long long *cycles, float *sink, long long iters, int blocks, int threads,
                              cudaStream_t st);
 

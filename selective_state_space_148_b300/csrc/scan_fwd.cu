@@ -89,6 +89,13 @@ static bool use_tmem_kernel() {
 
 cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long long Bsz, int grid_chunks,
                         cudaStream_t st) {
+    // the convolution-fed scan exists only in the tensor-memory kernel: never
+    // hand x to a kernel that would read it as u
+    if (a.conv_w != nullptr) {
+        if (!vec || a.flags != 0 || !use_tmem_kernel() || (a.nchunks > 1 && a.chunk_len % 32 != 0))
+            return cudaErrorNotSupported;
+        return launch_scan_tm(dtype, mode, a, Bsz, grid_chunks, st);
+    }
     // Its TMA boxes start on 32-step boundaries, so chunks must be whole
     // super-tiles; it declines (cudaErrorNotSupported) what its descriptors
     // cannot express and fp32 with N > 16.  N <= 8 keeps the shared-memory

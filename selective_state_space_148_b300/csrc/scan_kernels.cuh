@@ -50,6 +50,9 @@ struct ScanArgs {
     int nchunks;          // K
     int softplus;
     int flags;            // MAMBA_FLAG_ZOH (1) | MAMBA_FLAG_REVERSE (2); honoured by the GEN instantiation only
+    // non-null: `u` holds x and u = SiLU(causal width-4 conv of x) is formed in
+    // the kernel (tensor-memory kernel only): taps [Dch][4], bias [Dch] or null
+    const float *conv_w, *conv_b;
 };
 
 enum { SCAN_FLAG_ZOH = 1, SCAN_FLAG_REVERSE = 2 };

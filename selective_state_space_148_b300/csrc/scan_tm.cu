@@ -37,15 +37,15 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// [outer][mid][inner] tensor, box of 32 x box_mid x 1 elements
+// [outer][mid][inner] tensor, box of box_inner x box_mid x 1 elements
 bool encode_3d(CUtensorMap *m, const void *ptr, bool bf16, long long inner, long long mid, long long outer,
-               unsigned box_mid, bool swizzle) {
+               unsigned box_mid, bool swizzle, unsigned box_inner = 32) {
     const EncodeTiledFn fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t es = bf16 ? 2 : 4;
     const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)mid, (cuuint64_t)outer};
     const cuuint64_t strides[2] = {(cuuint64_t)inner * es, (cuuint64_t)inner * (cuuint64_t)mid * es};
-    const cuuint32_t box[3] = {32u, box_mid, 1u};
+    const cuuint32_t box[3] = {box_inner, box_mid, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     const CUtensorMapSwizzle sw =
         !swizzle ? CU_TENSOR_MAP_SWIZZLE_NONE : (bf16 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B);
@@ -86,11 +86,11 @@ int choose_warps(long long Bsz, long long Dch, int grid_chunks, int sms, int S) 
     return best;
 }
 
-template <typename T, int MODE, bool HAS_Z, int S>
+template <typename T, int MODE, bool HAS_Z, int S, bool CONV = false>
 cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int grid_chunks,
                           cudaStream_t st) {
-    using Sh = TmShape<T, MODE, S>;
-    auto kern = scan_tm_kernel<T, MODE, HAS_Z, S>;
+    using Sh = TmShape<T, MODE, S, CONV>;
+    auto kern = scan_tm_kernel<T, MODE, HAS_Z, S, CONV>;
     static bool attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -124,15 +124,23 @@ cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &a, long long Bsz
     // value) fit the selector's K = 16 for 4 lanes only
     const int S = a.N <= 16 ? 4 : a.N <= 32 ? 8 : 16;
     if (a.N > 64 || (!bf16 && S != 4)) return cudaErrorNotSupported;
+    // the convolution-fed variant is built for bf16, N <= 16, with the gate
+    const bool conv = a.conv_w != nullptr;
+    if (conv && (!bf16 || S != 4 || (mode == MODE_FULL && a.z == nullptr))) return cudaErrorNotSupported;
     const int warps = choose_warps(Bsz, a.Dch, grid_chunks, device_sms(), S);
     const unsigned ch = 32u * (unsigned)warps / (unsigned)S;
     TmMaps maps;
-    const bool ok = encode_3d(&maps.u, a.u, bf16, a.L, a.Dch, Bsz, ch, true) &&
+    const bool ok = (conv ? encode_3d(&maps.u, a.u, bf16, a.L, a.Dch, Bsz, ch, false, TmShape<bf16_t, MODE_FULL, 4, true>::XSTEPS)
+                          : encode_3d(&maps.u, a.u, bf16, a.L, a.Dch, Bsz, ch, true)) &&
                     encode_3d(&maps.delta, a.delta, bf16, a.L, a.Dch, Bsz, ch, true) &&
                     encode_3d(&maps.z, a.z != nullptr ? a.z : a.u, bf16, a.L, a.Dch, Bsz, ch, true) &&
                     encode_3d(&maps.B, a.Bm, bf16, a.L, a.N, Bsz, 4u * S, false) &&
                     encode_3d(&maps.C, a.Cm, bf16, a.L, a.N, Bsz, 4u * S, false);
     if (!ok) return cudaErrorNotSupported;
+    if (conv)
+        return mode == MODE_STATES
+                   ? launch_tm_one<bf16_t, MODE_STATES, false, 4, true>(a, maps, warps, Bsz, grid_chunks, st)
+                   : launch_tm_one<bf16_t, MODE_FULL, true, 4, true>(a, maps, warps, Bsz, grid_chunks, st);
     if (!bf16) return launch_tm_s<float, 4>(mode, a, maps, warps, Bsz, grid_chunks, st);
     switch (S) {
         case 4: return launch_tm_s<bf16_t, 4>(mode, a, maps, warps, Bsz, grid_chunks, st);

@@ -74,7 +74,9 @@ struct TmMaps {
 };
 
 // S = lanes per channel (4, 8 or 16: N <= 4 S), each lane owning 4 states.
-template <typename T, int MODE, int S_ = 4>
+// CONV: the first input tile is x with an 8-step halo (40 steps from t0 - 8,
+// unswizzled) from which u = SiLU(causal conv(x)) is formed.
+template <typename T, int MODE, int S_ = 4, bool CONV = false>
 struct TmShape {
     static constexpr int S = S_;
     static constexpr int MIN_WARPS = 8, MAX_WARPS = 12;  // CTA width, 32 / S channels per warp
@@ -90,7 +92,10 @@ struct TmShape {
     static constexpr int SWZ = ROW / 16;             // 16-byte chunks per swizzle span (64 B or 128 B)
     static constexpr int IO_TILE = (MAX_CH * ROW + 1023) / 1024 * 1024;  // slot of u, Delta_raw or z (box: 32 W / S rows)
     static constexpr int BC_TILE = 4 * S * ROW;      // one of B, C (box: 4 S state rows)
-    static constexpr int STAGE_BYTES = 3 * IO_TILE + 2 * BC_TILE;
+    static constexpr int XSTEPS = TT + 8;            // CONV: steps of the x box (8 of halo)
+    static constexpr int X0_TILE = CONV ? (MAX_CH * XSTEPS * (int)sizeof(T) + 1023) / 1024 * 1024 : IO_TILE;
+    static constexpr int OFF_BC = X0_TILE + 2 * IO_TILE;  // B then C, after u (or x), Delta_raw, z
+    static constexpr int STAGE_BYTES = OFF_BC + 2 * BC_TILE;
     static constexpr int A_BYTES = 128 * 16 * 2;
     static constexpr int X_BYTES = COLS * 16 * 2;
     static constexpr int DU_BYTES = MAX_CH * 4 * 16;           // per sub-tile: (Delta, Delta', du, du') per step pair
@@ -110,12 +115,14 @@ struct TmShape {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory");
 };
 
-// HAS_Z: the gate z is given (MODE_FULL only).  S lanes per channel.
+// HAS_Z: the gate z is given (MODE_FULL only).  S lanes per channel.  CONV:
+// a.u holds x and u = SiLU(a.conv_b + causal width-4 conv with a.conv_w) is
+// formed here (ai.xwebgame.com summary, "running it in PyTorch" block).
 // blockDim.x = 32 W, W in 8..12.
-template <typename T, int MODE, bool HAS_Z, int S_>
-__global__ void __launch_bounds__(TmShape<T, MODE, S_>::MAX_THR, 1)
+template <typename T, int MODE, bool HAS_Z, int S_, bool CONV = false>
+__global__ void __launch_bounds__(TmShape<T, MODE, S_, CONV>::MAX_THR, 1)
 scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
-    using Sh = TmShape<T, MODE, S_>;
+    using Sh = TmShape<T, MODE, S_, CONV>;
     constexpr bool FAST = sizeof(T) == 2;
     constexpr int S = Sh::S, TT = Sh::TT, TB = Sh::TB, NSUB = Sh::NSUB, COLS = Sh::COLS, MAX_CH = Sh::MAX_CH;
     constexpr int NST = Sh::NST;
@@ -198,6 +205,14 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     const float2 bias2 = f2(bias, bias);
     const float2 D2 = f2(Dd, Dd);
     const bool softplus = a.softplus != 0;
+    float4 cw = make_float4(0.f, 0.f, 0.f, 0.f);  // CONV: taps on x_{t-3}, ..., x_t
+    float cb = 0.f;
+    if constexpr (CONV) {
+        if (valid) {
+            cw = make_float4(a.conv_w[dd * 4], a.conv_w[dd * 4 + 1], a.conv_w[dd * 4 + 2], a.conv_w[dd * 4 + 3]);
+            cb = a.conv_b != nullptr ? a.conv_b[dd] : 0.f;
+        }
+    }
     // y of the step at offset r from t_begin in this lane's channel: ylane + r
     T *const ylane = reinterpret_cast<T *>(a.y) + ((b * a.Dch + dd) * L + t_begin);
 
@@ -217,12 +232,14 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         unsigned char *st = stage_of(sn % NST);
         uint64_t *bar = &io[sn % NST];
         const int x = (int)(t_begin + (long long)sn * TT);
-        tc::mbar_arrive_expect_tx(bar, (uint32_t)((HAS_Z ? 3 : 2) * ch * Sh::ROW + 2 * Sh::BC_TILE));
-        tc::tma_load_3d(st, &maps.u, x, (int)d0, (int)b, bar);
-        tc::tma_load_3d(st + Sh::IO_TILE, &maps.delta, x, (int)d0, (int)b, bar);
-        if (HAS_Z) tc::tma_load_3d(st + 2 * Sh::IO_TILE, &maps.z, x, (int)d0, (int)b, bar);
-        tc::tma_load_3d(st + 3 * Sh::IO_TILE, &maps.B, x, 0, (int)b, bar);  // 4 S state rows, zero past N
-        tc::tma_load_3d(st + 3 * Sh::IO_TILE + Sh::BC_TILE, &maps.C, x, 0, (int)b, bar);
+        const uint32_t first = CONV ? (uint32_t)(ch * Sh::XSTEPS * (int)sizeof(T)) : (uint32_t)(ch * Sh::ROW);
+        tc::mbar_arrive_expect_tx(bar, first + (uint32_t)((HAS_Z ? 2 : 1) * ch * Sh::ROW + 2 * Sh::BC_TILE));
+        // CONV: x from 8 steps back (a negative start reads zeros: the causal padding)
+        tc::tma_load_3d(st, &maps.u, CONV ? x - 8 : x, (int)d0, (int)b, bar);
+        tc::tma_load_3d(st + Sh::X0_TILE, &maps.delta, x, (int)d0, (int)b, bar);
+        if (HAS_Z) tc::tma_load_3d(st + Sh::X0_TILE + Sh::IO_TILE, &maps.z, x, (int)d0, (int)b, bar);
+        tc::tma_load_3d(st + Sh::OFF_BC, &maps.B, x, 0, (int)b, bar);  // 4 S state rows, zero past N
+        tc::tma_load_3d(st + Sh::OFF_BC + Sh::BC_TILE, &maps.C, x, 0, (int)b, bar);
     };
     int last_loaded = -1;  // thread 0: latest super-tile whose loads were issued
 
@@ -230,7 +247,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     // above), K row k = slice k's value (bf16), or K rows 3k..3k+2 its three
     // bf16 parts (fp32, S = 4)
     auto x_build = [&](int xb, const unsigned char *st) {
-        const T *raw = reinterpret_cast<const T *>(st + 3 * Sh::IO_TILE);  // [which][4 S][TT]
+        const T *raw = reinterpret_cast<const T *>(st + Sh::OFF_BC);  // [which][4 S][TT]
         unsigned char *xbase = sX + xb * Sh::X_BYTES;
         for (int n = tid; n < COLS; n += nthr) {
             const int j = n & 15;
@@ -290,8 +307,21 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         const int o = c * Sh::ROW + (q * TB + 2 * ps) * (int)sizeof(T);
         sw_off[q] = o ^ (((o >> 7) & (Sh::SWZ - 1)) << 4);
     }
+    // tensor 0 = u (or x), 1 = Delta_raw, 2 = z
     auto stage_word = [&](const unsigned char *st, int tensor, int q) -> Word {
-        return *reinterpret_cast<const Word *>(st + tensor * Sh::IO_TILE + sw_off[q]);
+        return *reinterpret_cast<const Word *>(st + (tensor == 0 ? 0 : Sh::X0_TILE + (tensor - 1) * Sh::IO_TILE) +
+                                               sw_off[q]);
+    };
+    // CONV: u of this lane's pair of sub-tile q, SiLU of the causal convolution
+    // of x; the x box holds steps t0 - 8 .. t0 + 31 of the super-tile unswizzled
+    auto conv_u = [&](const unsigned char *st, int q) -> float2 {
+        const T *xr = reinterpret_cast<const T *>(st) + c * Sh::XSTEPS + 8 + q * TB + 2 * ps;  // step t of the pair
+        const float2 m4 = unpack(*reinterpret_cast<const Word *>(xr - 4));  // x_{t-4}, x_{t-3}
+        const float2 m2 = unpack(*reinterpret_cast<const Word *>(xr - 2));  // x_{t-2}, x_{t-1}
+        const float2 m0 = unpack(*reinterpret_cast<const Word *>(xr));      // x_t, x_{t+1}
+        const float p0 = fmaf(cw.w, m0.x, fmaf(cw.z, m2.y, fmaf(cw.y, m2.x, fmaf(cw.x, m4.y, cb))));
+        const float p1 = fmaf(cw.w, m0.y, fmaf(cw.z, m0.x, fmaf(cw.y, m2.y, fmaf(cw.x, m2.x, cb))));
+        return silu2<FAST>(f2(p0, p1));
     };
     float4 *const du_chan = sDU + c * 4;  // + (i & 1) * MAX_CH * 4 + pair
     // Delta, Delta * u of this lane's pair at offset r (sub-tile parity par) ->
@@ -299,7 +329,9 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     float sdt_acc = 0.f;  // MODE_STATES: this lane's share of sum(Delta) over the chunk
     auto side_pair = [&](const unsigned char *st, int q, int r, int par, float2 &Du, float2 &g) {
         const bool in = (unsigned)r < lenv;
-        const float2 u = unpack(stage_word(st, 0, q));
+        float2 u;
+        if constexpr (CONV) u = conv_u(st, q);
+        else u = unpack(stage_word(st, 0, q));
         const float2 raw = __fadd2_rn(unpack(stage_word(st, 1, q)), bias2);
         float2 dl = softplus ? softplus2<FAST>(raw) : raw;
         dl = in ? dl : f2(0.f, 0.f);

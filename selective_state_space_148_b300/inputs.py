@@ -29,7 +29,7 @@ import os
 
 import numpy as np
 
-TAG_DT, TAG_D, TAG_U, TAG_DELTA, TAG_Z, TAG_B, TAG_C, TAG_STATE, TAG_EMBED, TAG_SYMBOLS = range(10)
+TAG_DT, TAG_D, TAG_U, TAG_DELTA, TAG_Z, TAG_B, TAG_C, TAG_STATE, TAG_EMBED, TAG_SYMBOLS, TAG_CONV_W, TAG_CONV_B = range(12)
 
 # Named workloads: (batch, d_inner, d_state, seq_len, io dtype, seed, u kind).
 WORKLOADS = {
@@ -107,6 +107,16 @@ def channel_params(dim: int, dstate: int, seed: int):
     D = _rng(seed, TAG_D).standard_normal(dim, dtype=np.float32)
     A = np.broadcast_to(-(np.arange(dstate, dtype=np.float32) + 1.0), (dim, dstate)).copy()
     return A, D, bias, dt
+
+
+def conv_params(dim: int, seed: int, width: int = 4):
+    """Depthwise causal conv taps [D, width] ~ N(0, 0.5) and bias [D] ~ N(0, 0.1), fp32.
+
+    The pages give no initialisation for the convolution branch; these keep SiLU(conv(x)) of
+    unit-scale x at the scale of the scan's u."""
+    w = (0.5 * _rng(seed, TAG_CONV_W).standard_normal((dim, width))).astype(np.float32)
+    b = (0.1 * _rng(seed, TAG_CONV_B).standard_normal(dim)).astype(np.float32)
+    return w, b
 
 
 @dataclasses.dataclass
