@@ -50,6 +50,8 @@ def _load():
                                               i64, i64, i64, i64]
         lib.oracle_state_update.restype = None
         lib.oracle_state_update.argtypes = [dp, dp, dp, dp, dp, dp, dp, dp, dp, ci, ci, dp, i64, i64, i64]
+        lib.oracle_selective_scan_bwd.restype = None
+        lib.oracle_selective_scan_bwd.argtypes = [dp] * 8 + [ci] + [dp] * 10 + [i64] * 4
         lib.oracle_causal_conv1d.restype = None
         lib.oracle_causal_conv1d.argtypes = [dp, dp, dp, ci, dp, i64, i64, i64, i64]
         lib.oracle_num_threads.restype = ci
@@ -143,3 +145,25 @@ def causal_conv1d(x, w, bias=None, silu=True):
     u = np.empty_like(x)
     _load().oracle_causal_conv1d(_ptr(x), _ptr(w), _ptr(b), int(bool(silu)), _ptr(u), Bsz * Dch, Dch, L, w.shape[1])
     return u
+
+
+def selective_scan_bwd(u, delta, A, B, C, dy, D=None, z=None, delta_bias=None, softplus_flag=True):
+    """Gradients of sum(dy * y) for the forward scan (simple discretisation, forward time, zero h0).
+
+    Returns a dict with du, ddelta [Bsz, Dch, L]; dA [Dch, N]; dB, dC [Bsz, N, L]; dD, ddelta_bias [Dch];
+    dz [Bsz, Dch, L] (None without a gate)."""
+    u, delta, A, B, C, dy = (_f64(a) for a in (u, delta, A, B, C, dy))
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    D = None if D is None else _f64(D)
+    z = None if z is None else _f64(z)
+    bias = None if delta_bias is None else _f64(delta_bias)
+    out = dict(du=np.empty_like(u), ddelta=np.empty_like(u), dA=np.empty((Dch, N)), dB=np.empty((Bsz, N, L)),
+               dC=np.empty((Bsz, N, L)), dD=np.empty(Dch), dz=np.empty_like(u) if z is not None else None,
+               ddelta_bias=np.empty(Dch))
+    work = np.empty((L + 1) * N + 2 * L + N)
+    _load().oracle_selective_scan_bwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(bias),
+                                      int(bool(softplus_flag)), _ptr(dy), _ptr(out["du"]), _ptr(out["ddelta"]),
+                                      _ptr(out["dA"]), _ptr(out["dB"]), _ptr(out["dC"]), _ptr(out["dD"]),
+                                      _ptr(out["dz"]), _ptr(out["ddelta_bias"]), _ptr(work), Bsz, Dch, L, N)
+    return out

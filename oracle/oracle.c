@@ -30,8 +30,9 @@
  *
  * Every function is sequential in t, in the order of the pages' step
  * function.  Parity status: pinned (LTI convolution, running sum, brute-force
- * unrolling, geometric closed form, hand-worked cases, invariants) -- see the
- * -m "not gpu" tests.
+ * unrolling, geometric closed form, hand-worked cases, invariants; the
+ * convolution branch against numpy's convolution; the backward pass against
+ * central differences of the forward) -- see the -m "not gpu" tests.
  */
 #include <math.h>
 #include <stddef.h>
@@ -158,6 +159,94 @@ void oracle_state_update(double *state, const double *u, const double *dt_raw,
 }
 
 /* Number of host threads the parallel loops above will use. */
+/*
+ * Gradient of the forward selective scan (simple discretisation, forward in
+ * time, zero initial state) for an upstream gradient dy of y.  The pages
+ * measure training throughput but print no backward pass; this is the chain
+ * rule applied to the [FS] §3.2 step as written in scan_channel, one channel
+ * at a time: a forward sweep that keeps every state h_t, then a sweep from
+ * t = L-1 down to 0 carrying dh = dLoss/dh_t:
+ *   g = SiLU(z_t) (1 without a gate),  dyh = dy_t * g,
+ *   dz_t = dy_t * yhat_t * SiLU'(z_t),  SiLU'(z) = s (1 + z (1 - s)), s = sigmoid(z)
+ *   dD += dyh u_t;  du_t = D dyh;  dC_{t,n} += dyh h_t[n];  dh[n] += dyh C_{t,n}
+ *   with a = exp(dt A_n), h_t = a h_{t-1} + dt B_{t,n} u_t:
+ *     dB_{t,n} += dh[n] dt u_t;  du_t += dh[n] dt B_{t,n}
+ *     ddt += dh[n] (B_{t,n} u_t + A_n a h_{t-1}[n]);  dA_n += dh[n] dt a h_{t-1}[n]
+ *     dh[n] *= a
+ *   ddt_raw_t = ddt * sigmoid(dt_raw_t + bias) (softplus) or ddt;  dbias += ddt_raw_t
+ * dA [Dch][N], dB, dC [Bsz][N][L], dD, dbias [Dch] are sums (zeroed here);
+ * du, ddt_raw [Bsz][Dch][L] and dz (when z is given) are per element.  Runs
+ * sequentially (the sums span channels).
+ */
+void oracle_selective_scan_bwd(const double *u, const double *dt_raw,
+                               const double *A, const double *Bm,
+                               const double *Cm, const double *Dv,
+                               const double *z, const double *bias,
+                               int softplus_flag, const double *dy, double *du,
+                               double *ddt_raw, double *dA, double *dB,
+                               double *dC, double *dD, double *dz,
+                               double *dbias, double *work, int64_t Bsz,
+                               int64_t Dch, int64_t L, int64_t N) {
+    /* work: (L + 1) * N + 2 * L + N doubles */
+    memset(dA, 0, sizeof(double) * Dch * N);
+    memset(dB, 0, sizeof(double) * Bsz * N * L);
+    memset(dC, 0, sizeof(double) * Bsz * N * L);
+    if (dD) memset(dD, 0, sizeof(double) * Dch);
+    if (dbias) memset(dbias, 0, sizeof(double) * Dch);
+    double *hs = work;                  /* hs[(t + 1) * N + n] = h_t[n], hs[n] = 0 */
+    double *dts = hs + (L + 1) * N;     /* Delta_t */
+    double *yh = dts + L;               /* y before the gate */
+    double *dh = yh + L;                /* N */
+    for (int64_t c = 0; c < Bsz * Dch; ++c) {
+        const int64_t b = c / Dch, d = c % Dch;
+        const double *uc = u + c * L, *rc = dt_raw + c * L, *zc = z ? z + c * L : NULL;
+        const double *Bb = Bm + b * N * L, *Cb = Cm + b * N * L, *Ad = A + d * N;
+        const double Dd = Dv ? Dv[d] : 0.0, bs = bias ? bias[d] : 0.0;
+        for (int64_t n = 0; n < N; ++n) hs[n] = 0.0;
+        for (int64_t t = 0; t < L; ++t) {
+            double dt = rc[t] + bs;
+            if (softplus_flag) dt = oracle_softplus(dt);
+            dts[t] = dt;
+            double acc = Dd * uc[t];
+            for (int64_t n = 0; n < N; ++n) {
+                const double h = exp(dt * Ad[n]) * hs[t * N + n] + dt * Bb[n * L + t] * uc[t];
+                hs[(t + 1) * N + n] = h;
+                acc += Cb[n * L + t] * h;
+            }
+            yh[t] = acc;
+        }
+        for (int64_t n = 0; n < N; ++n) dh[n] = 0.0;
+        for (int64_t t = L - 1; t >= 0; --t) {
+            const double dt = dts[t];
+            double g = 1.0;
+            if (zc) {
+                const double sg = 1.0 / (1.0 + exp(-zc[t]));
+                g = zc[t] * sg;
+                dz[c * L + t] = dy[c * L + t] * yh[t] * sg * (1.0 + zc[t] * (1.0 - sg));
+            }
+            const double dyh = dy[c * L + t] * g;
+            if (dD) dD[d] += dyh * uc[t];
+            double dut = Dd * dyh, ddt = 0.0;
+            for (int64_t n = 0; n < N; ++n) {
+                dC[(b * N + n) * L + t] += dyh * hs[(t + 1) * N + n];
+                dh[n] += dyh * Cb[n * L + t];
+            }
+            for (int64_t n = 0; n < N; ++n) {
+                const double a = exp(dt * Ad[n]), hp = hs[t * N + n];
+                dB[(b * N + n) * L + t] += dh[n] * dt * uc[t];
+                dut += dh[n] * dt * Bb[n * L + t];
+                ddt += dh[n] * (Bb[n * L + t] * uc[t] + Ad[n] * a * hp);
+                dA[d * N + n] += dh[n] * dt * a * hp;
+                dh[n] *= a;
+            }
+            du[c * L + t] = dut;
+            const double draw = softplus_flag ? ddt / (1.0 + exp(-(rc[t] + bs))) : ddt;
+            ddt_raw[c * L + t] = draw;
+            if (dbias) dbias[d] += draw;
+        }
+    }
+}
+
 /*
  * Depthwise causal convolution of width W followed by SiLU, per row
  * r = b * Dch + d of x [nrows][L]:

@@ -403,3 +403,64 @@ def test_conv_then_scan_composes_with_the_scan_oracle():
     y2, h2 = oracle.selective_scan(x / (1 + np.exp(-x)), delta, A, B, C)
     np.testing.assert_allclose(y1, y2, rtol=1e-13, atol=1e-13)
     np.testing.assert_allclose(h1, h2, rtol=1e-13, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- backward (chain rule of the forward scan)
+
+def _bwd_case(seed, Bsz=2, Dch=2, N=3, L=6):
+    r = np.random.default_rng(seed)
+    return dict(u=r.normal(size=(Bsz, Dch, L)), delta=r.normal(size=(Bsz, Dch, L)) - 1.0,
+                A=-r.uniform(0.5, 2.0, size=(Dch, N)), B=r.normal(size=(Bsz, N, L)), C=r.normal(size=(Bsz, N, L)),
+                D=r.normal(size=Dch), z=r.normal(size=(Bsz, Dch, L)), delta_bias=0.1 * r.normal(size=Dch),
+                dy=r.normal(size=(Bsz, Dch, L)))
+
+
+@pytest.mark.parametrize("gate,softplus", [(True, True), (False, True), (True, False)])
+def test_backward_matches_central_differences(gate, softplus):
+    """Every gradient of sum(dy * y) against central differences of the forward oracle (step 1e-6)."""
+    c = _bwd_case(7)
+    if not softplus:
+        c["delta"] = np.abs(c["delta"]) + 0.1          # Delta = Delta_raw + bias stays positive
+    z = c["z"] if gate else None
+    g = oracle.selective_scan_bwd(c["u"], c["delta"], c["A"], c["B"], c["C"], c["dy"], c["D"], z,
+                                  c["delta_bias"], softplus_flag=softplus)
+
+    def loss(**kw):
+        a = {k: c[k] for k in ("u", "delta", "A", "B", "C", "D", "delta_bias")}
+        a["z"] = z
+        a.update(kw)
+        y, _ = oracle.selective_scan(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["delta_bias"],
+                                     softplus_flag=softplus)
+        return float((c["dy"] * y).sum())
+
+    eps = 1e-6
+    names = [("u", "du"), ("delta", "ddelta"), ("A", "dA"), ("B", "dB"), ("C", "dC"), ("D", "dD"),
+             ("delta_bias", "ddelta_bias")] + ([("z", "dz")] if gate else [])
+    for name, key in names:
+        arr = c[name]
+        fd = np.zeros_like(arr)
+        for idx in np.ndindex(arr.shape):
+            p, m = arr.copy(), arr.copy()
+            p[idx] += eps
+            m[idx] -= eps
+            fd[idx] = (loss(**{name: p}) - loss(**{name: m})) / (2 * eps)
+        np.testing.assert_allclose(g[key], fd, rtol=1e-6, atol=1e-8, err_msg=key)
+    if not gate:
+        assert g["dz"] is None
+
+
+def test_backward_running_sum_closed_form():
+    """A = 0, Delta = 1 (softplus off), B = C = 1, D = 0, no gate: h_t[n] = sum_{s<=t} u_s and
+    y_t = N sum_{s<=t} u_s.  With dy = 1 at the last step only: du_s = N for every s, dB_{s,n} = u_s
+    (dh = 1 at every step) and dC is h_{L-1} = sum u at the last step, 0 elsewhere."""
+    Bsz, Dch, N, L = 1, 1, 4, 7
+    u = np.arange(1.0, L + 1).reshape(1, 1, L)
+    dy = np.zeros((1, 1, L))
+    dy[0, 0, -1] = 1.0
+    g = oracle.selective_scan_bwd(u, np.ones((1, 1, L)), np.zeros((1, N)), np.ones((1, N, L)), np.ones((1, N, L)), dy,
+                                  np.zeros(1), None, np.zeros(1), softplus_flag=False)
+    np.testing.assert_array_equal(g["du"], np.full((1, 1, L), float(N)))
+    np.testing.assert_array_equal(g["dB"], np.broadcast_to(u[:, :1, :], (1, N, L)))   # dh = 1 at every step
+    expect_dC = np.zeros((1, N, L))
+    expect_dC[0, :, -1] = u.sum()                                                    # h_{L-1} = sum u
+    np.testing.assert_array_equal(g["dC"], expect_dC)
