@@ -221,6 +221,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass of the scan (gradients of sum(dy * y)) on the workload")
     ap.add_argument("--conv", default="none", choices=["none", "fused", "two-step"],
                     help="feed the scan through the depthwise causal conv1d + SiLU branch: fused into the scan "
                          "kernel, or as a separate convolution launch before the scan")
@@ -249,6 +251,8 @@ def main():
     decode = args.workload == inputs.DECODE_WORKLOAD["name"]
     if decode:
         res = bench_decode(args, m, torch)
+    elif args.backward:
+        res = bench_backward(args, m, torch)
     else:
         res = bench_scan(args, m, torch)
 
@@ -258,7 +262,8 @@ def main():
     peaks = measured_peaks()
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not decode and args.conv == "none":
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not decode and args.conv == "none" and \
+            not args.backward:
         bps, ups, info = time_oracle(res["inputs"])
         cpu = {"value": bps / 1e9, "unit": "GB/s", "cores": info["threads"], "kind": "oracle",
                "sample": f"float64 oracle over whole time rows of {info['channels']} of {info['of']} channels "
@@ -267,7 +272,9 @@ def main():
 
     if rank == 0:
         line = {
-            "metric": METRIC if not decode else "selective_state_update achieved HBM GB/s and tokens/s",
+            "metric": ("selective_state_update achieved HBM GB/s and tokens/s" if decode else
+                       "selective_scan_bwd algorithmic HBM GB/s and (B·L) tokens/s per layer" if args.backward
+                       else METRIC),
             "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(t_ms, 6), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": res["dtype"], "data": "synthetic",
@@ -543,6 +550,96 @@ def bench_decode(args, m, torch):
                         "launch": f"the {args.steps} timed steps replayed as one captured CUDA graph"},
                 roofline=roof, h2d=h2d, d2h=d2h, e2e_ms=e2e_ms, launches=args.steps, clocks=cs.summary(),
                 mufu={"ex2_per_clk_per_sm": round(mufu_per_clk, 3), "sms": sms})
+
+
+def bwd_bytes(Bsz, Dch, L, N, io):
+    """Algorithmic bytes of the backward: read u, Delta_raw, z, dy, B, C; write du, ddelta, dz (storage type)
+    and dB, dC (fp32); parameters and their fp32 gradients."""
+    s = io_bytes(io)
+    return 7 * Bsz * Dch * L * s + 2 * Bsz * N * L * s + 2 * Bsz * N * L * 4 + 2 * Dch * N * 4 + 6 * Dch * 4
+
+
+def bench_backward(args, m, torch):
+    x = inputs.make_workload(args.workload)
+    Bsz, Dch, L, N = x.shape
+    io = x.io
+    dev = torch.device("cuda")
+
+    def d(a):
+        if io == "bf16":
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    dy_host = inputs._store(np.random.default_rng(11).standard_normal(x.u.shape).astype(np.float32), io)
+    t = dict(u=d(x.u), delta=d(x.delta), z=d(x.z), B=d(x.B), C=d(x.C), dy=d(dy_host))
+    A, D, bias = (torch.from_numpy(a).to(dev) for a in (x.A, x.D, x.delta_bias))
+    nbytes = bwd_bytes(Bsz, Dch, L, N, io)
+    R = max(2, math.ceil(3 * L2_BYTES / nbytes))
+    sets = [t] + [{k: v.clone() for k, v in t.items()} for _ in range(R - 1)]
+    f32 = dict(dtype=torch.float32, device=dev)
+    outs = [dict(du=torch.empty_like(t["u"]), dd=torch.empty_like(t["u"]), dz=torch.empty_like(t["u"]),
+                 dA=torch.empty((Dch, N), **f32), dB=torch.empty((Bsz, N, L), **f32),
+                 dC=torch.empty((Bsz, N, L), **f32), dD=torch.empty(Dch, **f32), db=torch.empty(Dch, **f32))
+            for _ in range(R)]
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        s, o = sets[i % R], outs[i % R]
+        m.mamba_selective_scan_bwd(s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, s["dy"], o["du"],
+                                   o["dd"], o["dA"], o["dB"], o["dC"], o["dD"], o["dz"], o["db"], stream=stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(pci_bus_id(torch)) as cs:
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    t_ms = ev0.elapsed_time(ev1) / args.steps
+
+    # end to end: inputs from pinned host memory, every gradient back to the host
+    hin = {k: v.cpu().pin_memory() for k, v in t.items()}
+    hout = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs[0].items()}
+
+    def e2e_step(i):
+        for k in t:
+            sets[0][k].copy_(hin[k], non_blocking=True)
+        step(0)
+        for k in hout:
+            hout[k].copy_(outs[0][k], non_blocking=True)
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    peaks = measured_peaks()
+    t_meas = t_ms * 1e-3
+    exps = Bsz * Dch * L * N
+    mufu_peak = SM_COUNT_NOMINAL * 32 * peaks["sm_max_mhz"] * 1e6
+    roof = {"bound": "alu", "achieved": round(exps / t_meas / 1e12, 4), "peak": round(mufu_peak / 1e12, 4),
+            "unit": "Tex2/s", "frac": round(exps / mufu_peak / t_meas, 4), "traffic": None,
+            "kernel": f"scan_bwd_kernel<{io},NS{4 if N <= 16 else 8 if N <= 32 else 16}>",
+            "note": "algorithmic exps count B·D·L·N once; the kernel evaluates them three times (checkpoint "
+                    "sweep, chunk recompute, reverse sweep)",
+            "hbm": {"achieved": round(nbytes / t_meas / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(nbytes / (peaks["hbm_gbs"] * 1e9) / t_meas, 4)}}
+    return dict(ms_per_step=t_ms, bytes=nbytes, tokens=Bsz * L, dtype="f32" if io == "f32" else "bf16",
+                config={"workload": args.workload, "pass": "backward", "batch": Bsz, "d_inner": Dch, "d_state": N,
+                        "seq_len": L, "io": io, "grads": "du, ddelta, dz (storage type); dA, dB, dC, dD, dbias fp32",
+                        "l2": f"inputs rotate over {R} resident copies"},
+                roofline=roof, h2d=sum(v.numel() * v.element_size() for v in hin.values()),
+                d2h=sum(v.numel() * v.element_size() for v in hout.values()), e2e_ms=e2e_ms,
+                launches=args.steps,  # the backward kernel (plus five cudaMemsetAsync zero fills per step)
+                clocks=cs.summary(), inputs=x)
 
 
 def reference_arm(args, world, rank):

@@ -154,6 +154,31 @@ int mamba_state_update(float *state, const void *u, const void *delta, const flo
                        int64_t Dch, int64_t N, int dtype, mamba_stream_t stream);
 
 /*
+ * Backward pass of the forward scan (simple discretisation B_bar = Delta B,
+ * forward time, zero initial state): gradients of sum(dy * y), the chain rule
+ * of the step in the fsdata.site explainer §3.2 (the pages measure training
+ * throughput but print no backward pass).
+ *
+ *   inputs      u, delta, A, B, C, D, z, delta_bias, softplus_flag as in
+ *               mamba_selective_scan_fwd; dy [Bsz][Dch][L] (dtype)
+ *   du, ddelta  [Bsz][Dch][L] (dtype): gradients for u and Delta_raw
+ *   dz          [Bsz][Dch][L] (dtype), required when z is given (else ignored)
+ *   dA [Dch][N], dB, dC [Bsz][N][L], dD [Dch], ddelta_bias [Dch]: fp32 sums,
+ *               written from zero by the call (dD, ddelta_bias may be NULL)
+ * States are recomputed from checkpoints taken every few steps; the
+ * checkpoints (Bsz*Dch*ceil(L/c)*N*4 bytes, c = 8, 4 or 2 for N <= 16, 32, 64)
+ * are allocated and freed stream-ordered inside the call.  dB and dC receive
+ * atomic additions, so their low-order bits may vary between runs.  Returns
+ * MAMBA_OK, MAMBA_ERR_NULL_ARG, MAMBA_ERR_BAD_SHAPE, MAMBA_ERR_UNSUPPORTED_N,
+ * MAMBA_ERR_BAD_DTYPE, MAMBA_ERR_ALLOC or MAMBA_ERR_LAUNCH.
+ */
+int mamba_selective_scan_bwd(const void *u, const void *delta, const float *A, const void *B, const void *C,
+                             const float *D, const void *z, const float *delta_bias, int softplus_flag,
+                             const void *dy, void *du, void *ddelta, float *dA, float *dB, float *dC, float *dD,
+                             void *dz, float *ddelta_bias, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
+                             int dtype, mamba_stream_t stream);
+
+/*
  * Depthwise causal convolution of width 4 followed by SiLU -- the branch that
  * turns x into the scan's input u (ai.xwebgame.com summary, "running it in
  * PyTorch" block: Conv1d(d_inner, d_inner, kernel_size=4, groups=d_inner,

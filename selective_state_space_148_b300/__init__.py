@@ -67,6 +67,8 @@ def lib() -> ctypes.CDLL:
         L.mamba_selective_scan_fwd_conv.restype = ci
         L.mamba_selective_scan_fwd_conv.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ci, vp, vp, i64, i64,
                                                     i64, i64, ci, vp]
+        L.mamba_selective_scan_bwd.restype = ci
+        L.mamba_selective_scan_bwd.argtypes = [vp] * 8 + [ci] + [vp] * 9 + [i64] * 4 + [ci, vp]
         L.mamba_bench_ex2.restype = ci
         L.mamba_bench_ex2.argtypes = [vp, vp, i64, ci, ci, vp]
         _lib = L
@@ -163,6 +165,19 @@ def mamba_selective_scan_fwd_conv(x, conv_w, conv_bias, delta, A, B, C, D, z, de
                                              _ptr(y), _ptr(last_state), Bsz, Dch, L, N, _dtype_code(x),
                                              _stream(stream))
     _check(st, "mamba_selective_scan_fwd_conv")
+
+
+def mamba_selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, ddelta, dA, dB, dC, dD, dz,
+                             ddelta_bias, stream=None):
+    """Gradients of sum(dy * y) of the forward scan (zero initial state).  du, ddelta, dz like u; dA [Dch, N],
+    dB, dC [Bsz, N, L], dD, ddelta_bias [Dch] fp32 (written from zero)."""
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    st = lib().mamba_selective_scan_bwd(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                        _ptr(delta_bias), int(bool(softplus_flag)), _ptr(dy), _ptr(du), _ptr(ddelta),
+                                        _ptr(dA), _ptr(dB), _ptr(dC), _ptr(dD), _ptr(dz), _ptr(ddelta_bias),
+                                        Bsz, Dch, L, N, _dtype_code(u), _stream(stream))
+    _check(st, "mamba_selective_scan_bwd")
 
 
 def mamba_scan_workspace_size(Bsz, Dch, L, N, chunk_len=0, dtype=MAMBA_BF16) -> int:

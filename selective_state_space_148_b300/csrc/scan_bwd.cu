@@ -1,0 +1,300 @@
+// scan_bwd.cu -- backward pass of the selective scan (simple discretisation,
+// forward time, zero initial state): gradients of sum(dy * y) for u, Delta_raw,
+// A, B, C, D, z and the Delta bias.
+//
+// The pages measure training throughput but print no backward pass; this is
+// the chain rule of the forward step (fsdata.site explainer §3.2 selective_step)
+// with, per (b, d, n), a sweep from t = L-1 down to 0 that carries
+// dh = dLoss/dh_t:
+//   dyh = dy_t g_t (g = SiLU(z_t), or 1),  dz_t = dy_t yhat_t SiLU'(z_t)
+//   dC_{t,n} += dyh h_t;  dh += dyh C_{t,n}
+//   a = exp(Delta A_n):  dB_{t,n} += dh Delta u_t,  du_t += dh Delta B_{t,n},
+//     dDelta_t += dh (B_{t,n} u_t + A_n a h_{t-1}),  dA_n += dh Delta a h_{t-1},  dh *= a
+//   du_t += D dyh,  dD += dyh u_t,  dDelta_raw_t = dDelta_t sigmoid(Delta_raw_t + bias),  dbias += dDelta_raw_t
+//
+// h_{t-1} is needed in reverse order, so states are recomputed by chunks: a
+// forward sweep writes the state at every chunk start (TC steps apart) to a
+// checkpoint workspace; then, chunk by chunk from the end, the chunk's states
+// are recomputed into shared memory from its checkpoint and swept in reverse.
+// Mapping: 4 lanes per channel, NS states per lane (N <= 4 NS), 32 channels
+// per CTA.  B and C are shared by every channel of a batch, so dB and dC are
+// sums over channels: each lane writes its per-step terms to shared memory,
+// the CTA sums them over its 32 channels at the end of a chunk and adds the
+// sums to dB, dC with one atomic add per CTA and element.  dA, dD and dbias
+// (sums over batches and steps) are kept in registers and added atomically at
+// the end.  No device-side waits.
+#include <cstdlib>
+#include <cstring>
+
+#include "../../include/mamba_scan.h"
+#include "internal.h"
+
+namespace mamba {
+
+struct BwdArgs {
+    const void *u, *delta, *z, *Bm, *Cm, *dy;
+    const float *A, *D, *bias;
+    void *du, *ddelta, *dz;
+    float *dA, *dB, *dC, *dD, *dbias;
+    float *ckpt;  // [Bsz][Dch][K][N]: state before step k * TC
+    long long Dch, L, N;
+    int softplus;
+};
+
+template <typename T, int NS>
+struct BwdShape {
+    static constexpr int S = 4, CH = 32, NTHR = S * CH;
+    static constexpr int TC = 32 / NS;  // steps per chunk: TC * NS = 32 states kept per lane
+    static constexpr int NP = S * NS;   // padded state count
+    // shared memory, floats: recomputed states [TC][NS][NTHR], dB and dC terms [TC][NS][NTHR] each
+    static constexpr int SH_FLOATS = TC * NS * NTHR;
+    static constexpr size_t SMEM_BYTES = 3 * SH_FLOATS * sizeof(float);
+};
+
+template <typename T, int NS>
+__global__ void __launch_bounds__(128)
+scan_bwd_kernel(const BwdArgs a, long long K) {
+    using Sh = BwdShape<T, NS>;
+    using IO = Io<T>;
+    constexpr int S = Sh::S, CH = Sh::CH, NTHR = Sh::NTHR, TC = Sh::TC;
+    extern __shared__ float4 smem_f4[];
+    float *const sH = reinterpret_cast<float *>(smem_f4);  // [TC][NS][NTHR]
+    float *const sdB = sH + Sh::SH_FLOATS;
+    float *const sdC = sdB + Sh::SH_FLOATS;
+
+    const int tid = threadIdx.x, s = tid & 3, c = tid >> 2;
+    const long long d = (long long)blockIdx.x * CH + c;
+    const bool valid = d < a.Dch;
+    const long long dd = valid ? d : 0;
+    const long long b = blockIdx.y;
+    const long long N = a.N, L = a.L;
+    const long long row = (b * a.Dch + dd) * L;
+    const long long bc0 = b * N * L;
+    const bool has_z = a.z != nullptr;
+
+    float An[NS], A2[NS], h[NS];
+    bool live[NS];
+#pragma unroll
+    for (int j = 0; j < NS; ++j) {
+        const long long n = (long long)s * NS + j;
+        live[j] = valid && n < N;
+        An[j] = live[j] ? a.A[dd * N + n] : 0.f;
+        A2[j] = An[j] * kLog2e;
+        h[j] = 0.f;
+    }
+    const float Dd = (a.D != nullptr && valid) ? a.D[dd] : 0.f;
+    const float bias = (a.bias != nullptr && valid) ? a.bias[dd] : 0.f;
+    auto delta_at = [&](long long t, float &raw) {
+        raw = valid ? IO::load(a.delta, row + t) + bias : 0.f;
+        return a.softplus ? softplus_f(raw) : raw;
+    };
+    auto bload = [&](const void *p, int j, long long t) {
+        return live[j] ? IO::load(p, bc0 + ((long long)s * NS + j) * L + t) : 0.f;
+    };
+    float *const ck = a.ckpt + ((b * a.Dch + dd) * K) * N + (long long)s * NS;
+
+    // ---- forward sweep: checkpoint the state before every chunk
+    for (long long t = 0; t < L; ++t) {
+        if (t % TC == 0) {
+#pragma unroll
+            for (int j = 0; j < NS; ++j)
+                if (live[j]) ck[(t / TC) * N + j] = h[j];
+        }
+        float raw;
+        const float dl = delta_at(t, raw);
+        const float du = dl * (valid ? IO::load(a.u, row + t) : 0.f);
+#pragma unroll
+        for (int j = 0; j < NS; ++j) h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * bload(a.Bm, j, t));
+    }
+
+    // ---- reverse sweep, chunk by chunk
+    float dh[NS], dAacc[NS];
+#pragma unroll
+    for (int j = 0; j < NS; ++j) dh[j] = dAacc[j] = 0.f;
+    float dDacc = 0.f, dbacc = 0.f;
+    for (long long k = K - 1; k >= 0; --k) {
+        const long long t0 = k * TC;
+        const int nt = (int)min((long long)TC, L - t0);
+        float hstart[NS];
+#pragma unroll
+        for (int j = 0; j < NS; ++j) h[j] = hstart[j] = live[j] ? ck[k * N + j] : 0.f;
+        for (int i = 0; i < nt; ++i) {  // recompute the chunk's states (private to this lane)
+            float raw;
+            const float dl = delta_at(t0 + i, raw);
+            const float du = dl * (valid ? IO::load(a.u, row + t0 + i) : 0.f);
+#pragma unroll
+            for (int j = 0; j < NS; ++j) {
+                h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * bload(a.Bm, j, t0 + i));
+                sH[(i * NS + j) * NTHR + tid] = h[j];
+            }
+        }
+        for (int i = nt - 1; i >= 0; --i) {
+            const long long t = t0 + i;
+            float raw;
+            const float dl = delta_at(t, raw);
+            const float uu = valid ? IO::load(a.u, row + t) : 0.f;
+            const float dyt = valid ? IO::load(a.dy, row + t) : 0.f;
+            // y before the gate, yhat = C . h_t + D u (its C . h part summed over the 4 lanes)
+            float ch = 0.f;
+#pragma unroll
+            for (int j = 0; j < NS; ++j) ch = fmaf(bload(a.Cm, j, t), sH[(i * NS + j) * NTHR + tid], ch);
+            float g = 1.f, dzt = 0.f;
+            if (has_z) {
+                ch += __shfl_xor_sync(0xffffffffu, ch, 1);
+                ch += __shfl_xor_sync(0xffffffffu, ch, 2);
+                const float zt = valid ? IO::load(a.z, row + t) : 0.f;
+                const float sg = 1.f / (1.f + __expf(-zt));
+                g = zt * sg;
+                dzt = dyt * fmaf(Dd, uu, ch) * sg * fmaf(zt, 1.f - sg, 1.f);
+            }
+            const float dyh = dyt * g;
+            float dup = 0.f, ddt = 0.f;
+#pragma unroll
+            for (int j = 0; j < NS; ++j) {
+                const float ht = sH[(i * NS + j) * NTHR + tid];
+                const float hp = i > 0 ? sH[((i - 1) * NS + j) * NTHR + tid] : hstart[j];
+                const float Bt = bload(a.Bm, j, t), Ct = bload(a.Cm, j, t);
+                sdC[(i * NS + j) * NTHR + tid] = dyh * ht;
+                dh[j] = fmaf(dyh, Ct, dh[j]);
+                const float e = ex2_approx(dl * A2[j]);
+                sdB[(i * NS + j) * NTHR + tid] = dh[j] * dl * uu;
+                dup = fmaf(dh[j] * dl, Bt, dup);
+                ddt = fmaf(dh[j], fmaf(Bt, uu, An[j] * e * hp), ddt);
+                dAacc[j] = fmaf(dh[j] * dl, e * hp, dAacc[j]);
+                dh[j] *= e;
+            }
+            dup += __shfl_xor_sync(0xffffffffu, dup, 1);
+            dup += __shfl_xor_sync(0xffffffffu, dup, 2);
+            ddt += __shfl_xor_sync(0xffffffffu, ddt, 1);
+            ddt += __shfl_xor_sync(0xffffffffu, ddt, 2);
+            if (valid && s == 0) {
+                const float draw = a.softplus ? ddt / (1.f + __expf(-raw)) : ddt;
+                IO::store(a.du, row + t, fmaf(Dd, dyh, dup));
+                IO::store(a.ddelta, row + t, draw);
+                if (has_z) IO::store(a.dz, row + t, dzt);
+                dDacc = fmaf(dyh, uu, dDacc);
+                dbacc += draw;
+            }
+        }
+        __syncthreads();
+        // dB, dC of this chunk: sum the CTA's channels, one atomic add per element
+        for (int q = tid; q < nt * S * NS; q += NTHR) {
+            const int i = q / (S * NS), n = q % (S * NS);  // state n = s' * NS + j
+            const int sl = n / NS, j = n % NS;
+            if (n < N) {
+                float sb = 0.f, sc = 0.f;
+                for (int cc = 0; cc < CH; ++cc) {
+                    sb += sdB[(i * NS + j) * NTHR + cc * S + sl];
+                    sc += sdC[(i * NS + j) * NTHR + cc * S + sl];
+                }
+                atomicAdd(a.dB + bc0 + (long long)n * L + t0 + i, sb);
+                atomicAdd(a.dC + bc0 + (long long)n * L + t0 + i, sc);
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int j = 0; j < NS; ++j)
+        if (live[j]) atomicAdd(a.dA + dd * N + (long long)s * NS + j, dAacc[j]);
+    if (valid && s == 0) {
+        if (a.dD != nullptr) atomicAdd(a.dD + dd, dDacc);
+        if (a.dbias != nullptr) atomicAdd(a.dbias + dd, dbacc);
+    }
+}
+
+template <typename T, int NS>
+static cudaError_t launch_bwd_ns(const BwdArgs &a, long long Bsz, long long K, cudaStream_t st) {
+    using Sh = BwdShape<T, NS>;
+    auto kern = scan_bwd_kernel<T, NS>;
+    if (Sh::SMEM_BYTES > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+    }
+    dim3 grid((unsigned)((a.Dch + Sh::CH - 1) / Sh::CH), (unsigned)Bsz, 1);
+    kern<<<grid, Sh::NTHR, Sh::SMEM_BYTES, st>>>(a, K);
+    return cudaGetLastError();
+}
+
+// steps per checkpoint chunk for N states
+int bwd_chunk_steps(long long N) { return N <= 16 ? 8 : N <= 32 ? 4 : 2; }
+
+cudaError_t launch_scan_bwd(int dtype, const BwdArgs &a, long long Bsz, cudaStream_t st) {
+    const long long K = (a.L + bwd_chunk_steps(a.N) - 1) / bwd_chunk_steps(a.N);
+    if (dtype == 1) {
+        if (a.N <= 16) return launch_bwd_ns<bf16_t, 4>(a, Bsz, K, st);
+        if (a.N <= 32) return launch_bwd_ns<bf16_t, 8>(a, Bsz, K, st);
+        return launch_bwd_ns<bf16_t, 16>(a, Bsz, K, st);
+    }
+    if (a.N <= 16) return launch_bwd_ns<float, 4>(a, Bsz, K, st);
+    if (a.N <= 32) return launch_bwd_ns<float, 8>(a, Bsz, K, st);
+    return launch_bwd_ns<float, 16>(a, Bsz, K, st);
+}
+
+}  // namespace mamba
+
+// ---------------------------------------------------------------------------- C ABI
+
+extern "C" int mamba_selective_scan_bwd(const void *u, const void *delta, const float *A, const void *B,
+                                        const void *C, const float *D, const void *z, const float *delta_bias,
+                                        int softplus_flag, const void *dy, void *du, void *ddelta, float *dA,
+                                        float *dB, float *dC, float *dD, void *dz, float *ddelta_bias, int64_t Bsz,
+                                        int64_t Dch, int64_t L, int64_t N, int dtype, mamba_stream_t stream) {
+    using namespace mamba;
+    if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC) return MAMBA_ERR_NULL_ARG;
+    if (z != nullptr && dz == nullptr) return MAMBA_ERR_NULL_ARG;
+    if (dtype != MAMBA_F32 && dtype != MAMBA_BF16) return MAMBA_ERR_BAD_DTYPE;
+    constexpr long long kMax = 1LL << 40;
+    if (Bsz <= 0 || Dch <= 0 || L <= 0 || N <= 0 || Bsz > 65535 || Dch > kMax || L > kMax ||
+        Bsz * Dch > kMax / L || Bsz * N > kMax / L)
+        return MAMBA_ERR_BAD_SHAPE;
+    if (N > 64) return MAMBA_ERR_UNSUPPORTED_N;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const long long K = (L + bwd_chunk_steps(N) - 1) / bwd_chunk_steps(N);
+    const size_t ck_bytes = (size_t)(Bsz * Dch) * (size_t)K * (size_t)N * sizeof(float);
+    void *ck = nullptr;
+    const char *inject = std::getenv("MAMBA_FAULT_INJECT");  // host-side test hook, as in the forward scan
+    if (inject != nullptr && std::strcmp(inject, "alloc") == 0) return MAMBA_ERR_ALLOC;
+    if (cudaMallocAsync(&ck, ck_bytes, st) != cudaSuccess) {
+        cudaGetLastError();
+        return MAMBA_ERR_ALLOC;
+    }
+    int rc = MAMBA_OK;
+    // the sums start from zero
+    if (cudaMemsetAsync(dA, 0, (size_t)(Dch * N) * sizeof(float), st) != cudaSuccess ||
+        cudaMemsetAsync(dB, 0, (size_t)(Bsz * N * L) * sizeof(float), st) != cudaSuccess ||
+        cudaMemsetAsync(dC, 0, (size_t)(Bsz * N * L) * sizeof(float), st) != cudaSuccess ||
+        (dD != nullptr && cudaMemsetAsync(dD, 0, (size_t)Dch * sizeof(float), st) != cudaSuccess) ||
+        (ddelta_bias != nullptr && cudaMemsetAsync(ddelta_bias, 0, (size_t)Dch * sizeof(float), st) != cudaSuccess))
+        rc = MAMBA_ERR_LAUNCH;
+    if (rc == MAMBA_OK) {
+        BwdArgs a{};
+        a.u = u;
+        a.delta = delta;
+        a.z = z;
+        a.Bm = B;
+        a.Cm = C;
+        a.dy = dy;
+        a.A = A;
+        a.D = D;
+        a.bias = delta_bias;
+        a.du = du;
+        a.ddelta = ddelta;
+        a.dz = dz;
+        a.dA = dA;
+        a.dB = dB;
+        a.dC = dC;
+        a.dD = dD;
+        a.dbias = ddelta_bias;
+        a.ckpt = static_cast<float *>(ck);
+        a.Dch = Dch;
+        a.L = L;
+        a.N = N;
+        a.softplus = softplus_flag ? 1 : 0;
+        if (launch_scan_bwd(dtype, a, Bsz, st) != cudaSuccess) rc = MAMBA_ERR_LAUNCH;
+    }
+    if (cudaFreeAsync(ck, st) != cudaSuccess) {
+        cudaGetLastError();
+        if (rc == MAMBA_OK) rc = MAMBA_ERR_LAUNCH;
+    }
+    return rc;
+}
