@@ -323,12 +323,16 @@ def traffic_record(kernel_key):
     return rec.get("dram_bytes_per_launch")
 
 
+# the sources the forward scan kernels are built from (a change to any of them voids a stored ncu record)
+SCAN_KERNEL_SOURCES = ("scan_tm.cuh", "scan_tm.cu", "tcgen05.cuh", "common.cuh", "scan_kernels.cuh", "scan_fwd.cu",
+                       "internal.h")
+
+
 def kernel_source_sha():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_148_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in SCAN_KERNEL_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
