@@ -17,7 +17,10 @@
 // checkpoint workspace; then, chunk by chunk from the end, the chunk's states
 // are recomputed into shared memory from its checkpoint and swept in reverse.
 // Mapping: 4 lanes per channel, NS states per lane (N <= 4 NS), 32 channels
-// per CTA.  B and C are shared by every channel of a batch, so dB and dC are
+// per CTA.  Each chunk's inputs (u, Delta_raw, z, dy rows of the CTA's
+// channels, B and C rows) are staged in shared memory with coalesced loads, and
+// its du, ddelta, dz rows leave through shared memory the same way.  B and C
+// are shared by every channel of a batch, so dB and dC are
 // sums over channels: each lane writes its per-step terms to shared memory,
 // the CTA sums them over its 32 channels at the end of a chunk and adds the
 // sums to dB, dC with one atomic add per CTA and element.  dA, dD and dbias
@@ -46,9 +49,11 @@ struct BwdShape {
     static constexpr int S = 4, CH = 32, NTHR = S * CH;
     static constexpr int TC = 32 / NS;  // steps per chunk: TC * NS = 32 states kept per lane
     static constexpr int NP = S * NS;   // padded state count
-    // shared memory, floats: recomputed states [TC][NS][NTHR], dB and dC terms [TC][NS][NTHR] each
+    // shared memory, floats: recomputed states [TC][NS][NTHR] and the dB, dC terms [TC][NS][NTHR] each;
+    // the chunk's inputs u, Delta_raw, z, dy [4][CH][TC] and B, C [2][TC][NP]; outputs du, ddelta, dz [3][CH][TC]
     static constexpr int SH_FLOATS = TC * NS * NTHR;
-    static constexpr size_t SMEM_BYTES = 3 * SH_FLOATS * sizeof(float);
+    static constexpr int IN_FLOATS = 4 * CH * TC, BC_FLOATS = 2 * TC * NP, OUT_FLOATS = 3 * CH * TC;
+    static constexpr size_t SMEM_BYTES = (3 * SH_FLOATS + IN_FLOATS + BC_FLOATS + OUT_FLOATS) * sizeof(float);
 };
 
 template <typename T, int NS>
@@ -56,11 +61,14 @@ __global__ void __launch_bounds__(128)
 scan_bwd_kernel(const BwdArgs a, long long K) {
     using Sh = BwdShape<T, NS>;
     using IO = Io<T>;
-    constexpr int S = Sh::S, CH = Sh::CH, NTHR = Sh::NTHR, TC = Sh::TC;
+    constexpr int S = Sh::S, CH = Sh::CH, NTHR = Sh::NTHR, TC = Sh::TC, NP = Sh::NP;
     extern __shared__ float4 smem_f4[];
     float *const sH = reinterpret_cast<float *>(smem_f4);  // [TC][NS][NTHR]
     float *const sdB = sH + Sh::SH_FLOATS;
     float *const sdC = sdB + Sh::SH_FLOATS;
+    float *const sIn = sdC + Sh::SH_FLOATS;    // [4][CH][TC]: u, Delta_raw, z, dy
+    float *const sBC = sIn + Sh::IN_FLOATS;    // [2][TC][NP]: B, C
+    float *const sOut = sBC + Sh::BC_FLOATS;   // [3][CH][TC]: du, ddelta, dz
 
     const int tid = threadIdx.x, s = tid & 3, c = tid >> 2;
     const long long d = (long long)blockIdx.x * CH + c;
@@ -68,7 +76,6 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
     const long long dd = valid ? d : 0;
     const long long b = blockIdx.y;
     const long long N = a.N, L = a.L;
-    const long long row = (b * a.Dch + dd) * L;
     const long long bc0 = b * N * L;
     const bool has_z = a.z != nullptr;
 
@@ -84,27 +91,71 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
     }
     const float Dd = (a.D != nullptr && valid) ? a.D[dd] : 0.f;
     const float bias = (a.bias != nullptr && valid) ? a.bias[dd] : 0.f;
-    auto delta_at = [&](long long t, float &raw) {
-        raw = valid ? IO::load(a.delta, row + t) + bias : 0.f;
-        return a.softplus ? softplus_f(raw) : raw;
-    };
-    auto bload = [&](const void *p, int j, long long t) {
-        return live[j] ? IO::load(p, bc0 + ((long long)s * NS + j) * L + t) : 0.f;
-    };
     float *const ck = a.ckpt + ((b * a.Dch + dd) * K) * N + (long long)s * NS;
+    const float *const in_u = sIn + c * TC, *const in_r = sIn + (CH + c) * TC;
+    const float *const in_z = sIn + (2 * CH + c) * TC, *const in_dy = sIn + (3 * CH + c) * TC;
 
-    // ---- forward sweep: checkpoint the state before every chunk
-    for (long long t = 0; t < L; ++t) {
-        if (t % TC == 0) {
+    // Inputs of steps t0 .. t0 + nt - 1 (zero past the end, past Dch, past N): loaded into registers one
+    // chunk ahead (load_chunk), written to shared memory when the chunk starts (store_chunk).  ntens = 2: u
+    // and Delta_raw with B (the forward sweep); 4: also z and dy, with B and C.
+    constexpr int PT = TC, PB = 2;  // elements per thread: 4 * CH * TC / NTHR and 2 * NP * TC / NTHR
+    static_assert(4 * CH * TC == PT * NTHR && 2 * NP * TC == PB * NTHR, "staging splits evenly");
+    float pt[PT], pb[PB];
+    auto load_chunk = [&](long long t0, int nt, int ntens) {
 #pragma unroll
-            for (int j = 0; j < NS; ++j)
-                if (live[j]) ck[(t / TC) * N + j] = h[j];
+        for (int r = 0; r < PT; ++r) {
+            const int q = tid + r * NTHR;
+            const int tens = q / (CH * TC), cc = (q / TC) % CH, i = q % TC;
+            const long long dch = (long long)blockIdx.x * CH + cc;
+            const void *p = tens == 0 ? a.u : tens == 1 ? a.delta : tens == 2 ? a.z : a.dy;
+            float v = 0.f;
+            if (tens < ntens && i < nt && dch < a.Dch && p != nullptr) v = IO::load(p, (b * a.Dch + dch) * L + t0 + i);
+            pt[r] = v;
         }
-        float raw;
-        const float dl = delta_at(t, raw);
-        const float du = dl * (valid ? IO::load(a.u, row + t) : 0.f);
 #pragma unroll
-        for (int j = 0; j < NS; ++j) h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * bload(a.Bm, j, t));
+        for (int r = 0; r < PB; ++r) {
+            const int q = tid + r * NTHR;
+            const int which = q / (NP * TC), n = (q / TC) % NP, i = q % TC;
+            float v = 0.f;
+            if ((which == 0 || ntens == 4) && i < nt && n < N)
+                v = IO::load(which ? a.Cm : a.Bm, bc0 + (long long)n * L + t0 + i);
+            pb[r] = v;
+        }
+    };
+    auto store_chunk = [&]() {
+#pragma unroll
+        for (int r = 0; r < PT; ++r) sIn[tid + r * NTHR] = pt[r];
+#pragma unroll
+        for (int r = 0; r < PB; ++r) {
+            const int q = tid + r * NTHR;
+            const int which = q / (NP * TC), n = (q / TC) % NP, i = q % TC;
+            sBC[(which * TC + i) * NP + n] = pb[r];
+        }
+    };
+    auto softplus_of = [&](float raw) { return a.softplus ? softplus_f(raw) : raw; };
+
+    auto chunk_len = [&](long long k) { return (int)min((long long)TC, L - k * TC); };
+    // ---- forward sweep: checkpoint the state before every chunk
+    load_chunk(0, chunk_len(0), 2);
+    for (long long k = 0; k < K; ++k) {
+        const int nt = chunk_len(k);
+#pragma unroll
+        for (int j = 0; j < NS; ++j)
+            if (live[j]) ck[k * N + j] = h[j];
+        __syncthreads();
+        store_chunk();
+        __syncthreads();
+        if (k + 1 < K) load_chunk((k + 1) * TC, chunk_len(k + 1), 2);  // in flight during this chunk
+#pragma unroll
+        for (int i = 0; i < TC; ++i) {
+            if (i < nt) {
+                const float dl = softplus_of(in_r[i] + bias);
+                const float du = dl * in_u[i];
+#pragma unroll
+                for (int j = 0; j < NS; ++j)
+                    h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * sBC[i * NP + s * NS + j]);
+            }
+        }
     }
 
     // ---- reverse sweep, chunk by chunk
@@ -112,37 +163,53 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
 #pragma unroll
     for (int j = 0; j < NS; ++j) dh[j] = dAacc[j] = 0.f;
     float dDacc = 0.f, dbacc = 0.f;
+    float hnext[NS];  // checkpoint of the next chunk to process, loaded one chunk ahead
+    load_chunk((K - 1) * TC, chunk_len(K - 1), 4);
+#pragma unroll
+    for (int j = 0; j < NS; ++j) hnext[j] = live[j] ? ck[(K - 1) * N + j] : 0.f;
     for (long long k = K - 1; k >= 0; --k) {
         const long long t0 = k * TC;
-        const int nt = (int)min((long long)TC, L - t0);
-        float hstart[NS];
+        const int nt = chunk_len(k);
+        __syncthreads();
+        store_chunk();
+        __syncthreads();
+        float hstart[NS], dlr[TC];
 #pragma unroll
-        for (int j = 0; j < NS; ++j) h[j] = hstart[j] = live[j] ? ck[k * N + j] : 0.f;
-        for (int i = 0; i < nt; ++i) {  // recompute the chunk's states (private to this lane)
-            float raw;
-            const float dl = delta_at(t0 + i, raw);
-            const float du = dl * (valid ? IO::load(a.u, row + t0 + i) : 0.f);
+        for (int j = 0; j < NS; ++j) h[j] = hstart[j] = hnext[j];
+        if (k > 0) {  // in flight during this chunk
+            load_chunk((k - 1) * TC, TC, 4);
 #pragma unroll
-            for (int j = 0; j < NS; ++j) {
-                h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * bload(a.Bm, j, t0 + i));
-                sH[(i * NS + j) * NTHR + tid] = h[j];
+            for (int j = 0; j < NS; ++j) hnext[j] = live[j] ? ck[(k - 1) * N + j] : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < TC; ++i) {  // recompute the chunk's states (private to this lane)
+            dlr[i] = 0.f;
+            if (i < nt) {
+                const float dl = softplus_of(in_r[i] + bias);
+                dlr[i] = dl;
+                const float du = dl * in_u[i];
+#pragma unroll
+                for (int j = 0; j < NS; ++j) {
+                    h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * sBC[i * NP + s * NS + j]);
+                    sH[(i * NS + j) * NTHR + tid] = h[j];
+                }
             }
         }
-        for (int i = nt - 1; i >= 0; --i) {
-            const long long t = t0 + i;
-            float raw;
-            const float dl = delta_at(t, raw);
-            const float uu = valid ? IO::load(a.u, row + t) : 0.f;
-            const float dyt = valid ? IO::load(a.dy, row + t) : 0.f;
-            // y before the gate, yhat = C . h_t + D u (its C . h part summed over the 4 lanes)
-            float ch = 0.f;
 #pragma unroll
-            for (int j = 0; j < NS; ++j) ch = fmaf(bload(a.Cm, j, t), sH[(i * NS + j) * NTHR + tid], ch);
+        for (int i = TC - 1; i >= 0; --i) {
+            if (i >= nt) continue;
+            const float dl = dlr[i];
+            const float raw = in_r[i] + bias;
+            const float uu = in_u[i], dyt = in_dy[i];
+            const float *Bt = sBC + i * NP + s * NS, *Ct = sBC + (TC + i) * NP + s * NS;
             float g = 1.f, dzt = 0.f;
-            if (has_z) {
+            if (has_z) {  // yhat = C . h_t + D u, the C . h part summed over the 4 lanes
+                float ch = 0.f;
+#pragma unroll
+                for (int j = 0; j < NS; ++j) ch = fmaf(Ct[j], sH[(i * NS + j) * NTHR + tid], ch);
                 ch += __shfl_xor_sync(0xffffffffu, ch, 1);
                 ch += __shfl_xor_sync(0xffffffffu, ch, 2);
-                const float zt = valid ? IO::load(a.z, row + t) : 0.f;
+                const float zt = in_z[i];
                 const float sg = 1.f / (1.f + __expf(-zt));
                 g = zt * sg;
                 dzt = dyt * fmaf(Dd, uu, ch) * sg * fmaf(zt, 1.f - sg, 1.f);
@@ -153,13 +220,12 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
             for (int j = 0; j < NS; ++j) {
                 const float ht = sH[(i * NS + j) * NTHR + tid];
                 const float hp = i > 0 ? sH[((i - 1) * NS + j) * NTHR + tid] : hstart[j];
-                const float Bt = bload(a.Bm, j, t), Ct = bload(a.Cm, j, t);
                 sdC[(i * NS + j) * NTHR + tid] = dyh * ht;
-                dh[j] = fmaf(dyh, Ct, dh[j]);
+                dh[j] = fmaf(dyh, Ct[j], dh[j]);
                 const float e = ex2_approx(dl * A2[j]);
                 sdB[(i * NS + j) * NTHR + tid] = dh[j] * dl * uu;
-                dup = fmaf(dh[j] * dl, Bt, dup);
-                ddt = fmaf(dh[j], fmaf(Bt, uu, An[j] * e * hp), ddt);
+                dup = fmaf(dh[j] * dl, Bt[j], dup);
+                ddt = fmaf(dh[j], fmaf(Bt[j], uu, An[j] * e * hp), ddt);
                 dAacc[j] = fmaf(dh[j] * dl, e * hp, dAacc[j]);
                 dh[j] *= e;
             }
@@ -167,19 +233,28 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
             dup += __shfl_xor_sync(0xffffffffu, dup, 2);
             ddt += __shfl_xor_sync(0xffffffffu, ddt, 1);
             ddt += __shfl_xor_sync(0xffffffffu, ddt, 2);
-            if (valid && s == 0) {
+            if (s == 0) {
                 const float draw = a.softplus ? ddt / (1.f + __expf(-raw)) : ddt;
-                IO::store(a.du, row + t, fmaf(Dd, dyh, dup));
-                IO::store(a.ddelta, row + t, draw);
-                if (has_z) IO::store(a.dz, row + t, dzt);
-                dDacc = fmaf(dyh, uu, dDacc);
-                dbacc += draw;
+                sOut[c * TC + i] = fmaf(Dd, dyh, dup);
+                sOut[(CH + c) * TC + i] = draw;
+                sOut[(2 * CH + c) * TC + i] = dzt;
+                if (valid) {
+                    dDacc = fmaf(dyh, uu, dDacc);
+                    dbacc += draw;
+                }
             }
         }
         __syncthreads();
-        // dB, dC of this chunk: sum the CTA's channels, one atomic add per element
-        for (int q = tid; q < nt * S * NS; q += NTHR) {
-            const int i = q / (S * NS), n = q % (S * NS);  // state n = s' * NS + j
+        // this chunk's du, ddelta, dz rows, and dB, dC summed over the CTA's channels (one atomic add
+        // per CTA and element)
+        for (int q = tid; q < (has_z ? 3 : 2) * CH * TC; q += NTHR) {
+            const int tens = q / (CH * TC), cc = (q / TC) % CH, i = q % TC;
+            const long long dch = (long long)blockIdx.x * CH + cc;
+            if (i < nt && dch < a.Dch)
+                IO::store(tens == 0 ? a.du : tens == 1 ? a.ddelta : a.dz, (b * a.Dch + dch) * L + t0 + i, sOut[q]);
+        }
+        for (int q = tid; q < nt * NP; q += NTHR) {
+            const int i = q / NP, n = q % NP;  // state n = s' * NS + j
             const int sl = n / NS, j = n % NS;
             if (n < N) {
                 float sb = 0.f, sc = 0.f;
@@ -191,7 +266,6 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
                 atomicAdd(a.dC + bc0 + (long long)n * L + t0 + i, sc);
             }
         }
-        __syncthreads();
     }
 #pragma unroll
     for (int j = 0; j < NS; ++j)
