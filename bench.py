@@ -296,6 +296,43 @@ def main():
         dist.destroy_process_group()
 
 
+def pipelined_e2e(torch, steps, upload, compute, download, nbuf=2):
+    """Time `steps` end-to-end steps (ms per step): step i uploads its inputs from pinned host memory into
+    device buffer set i % nbuf, computes, and downloads its results, on three streams so that the upload of
+    step i+1 and the download of step i-1 overlap the compute of step i.  Every step still moves all of its
+    bytes inside the timed region.  upload/compute/download(k, stream) enqueue work for buffer set k."""
+    main = torch.cuda.current_stream()
+    up, comp, down = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev = {n: [torch.cuda.Event() for _ in range(nbuf)] for n in ("up", "comp", "down")}
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(main)
+    for st in (up, comp, down):
+        st.wait_stream(main)
+    for i in range(steps):
+        k = i % nbuf
+        with torch.cuda.stream(up):
+            if i >= nbuf:
+                up.wait_event(ev["comp"][k])          # the compute that read buffer set k is done
+            upload(k, up)
+            ev["up"][k].record(up)
+        with torch.cuda.stream(comp):
+            comp.wait_event(ev["up"][k])
+            if i >= nbuf:
+                comp.wait_event(ev["down"][k])        # the results in buffer set k have been read back
+            compute(k, comp)
+            ev["comp"][k].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(ev["comp"][k])
+            download(k, down)
+            ev["down"][k].record(down)
+    for st in (up, comp, down):
+        main.wait_stream(st)
+    t1.record(main)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps
+
+
 def max_over_ranks(values, dist, torch, device):
     """Element-wise maximum over all ranks (the identity without a process group)."""
     if dist is None:
@@ -364,15 +401,17 @@ def bench_scan(args, m, torch):
         cw, cb = (torch.from_numpy(a).to(dev) for a in inputs.conv_params(Dch, 7))
         u_tmp = torch.empty_like(base["u"])
 
-    def run(s, y, h):
+    def run(s, y, h, st=None, ut=None):
+        st = stream if st is None else st
+        ut = u_tmp if ut is None and args.conv == "two-step" else ut
         if args.conv == "fused":
             m.mamba_selective_scan_fwd_conv(s["u"], cw, cb, s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h,
-                                            stream=stream)
+                                            stream=st)
         elif args.conv == "two-step":
-            m.mamba_causal_conv1d_silu(s["u"], cw, cb, 1, u_tmp, stream=stream)
-            m.mamba_selective_scan_fwd(u_tmp, s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h, stream=stream)
+            m.mamba_causal_conv1d_silu(s["u"], cw, cb, 1, ut, stream=st)
+            m.mamba_selective_scan_fwd(ut, s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h, stream=st)
         else:
-            m.mamba_selective_scan_fwd(s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h, stream=stream)
+            m.mamba_selective_scan_fwd(s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h, stream=st)
 
     def step(i):
         run(sets[i % R], ys[i % R], hs[i % R])
@@ -392,31 +431,29 @@ def bench_scan(args, m, torch):
     t_ms = ev0.elapsed_time(ev1) / args.steps
     clocks = cs.summary()
 
-    # end to end through the C ABI from pinned host buffers
+    # end to end through the C ABI from pinned host buffers (uploads and downloads overlap the neighbouring
+    # steps' kernels; two device buffer sets)
     hsrc = {k: v.cpu().pin_memory() for k, v in base.items()}
-    hy = torch.empty(base["u"].shape, dtype=tdt).pin_memory()
-    hh = torch.empty((Bsz, Dch, N), dtype=torch.float32).pin_memory()
-    dsets = sets[0]
+    hy = [torch.empty(base["u"].shape, dtype=tdt).pin_memory() for _ in range(2)]
+    hh = [torch.empty((Bsz, Dch, N), dtype=torch.float32).pin_memory() for _ in range(2)]
+    dsets = [sets[0], sets[1]]
+    utmp = [torch.empty_like(base["u"]) for _ in range(2)] if args.conv == "two-step" else [None, None]
 
-    def e2e_step(i):
-        for k in dsets:
-            dsets[k].copy_(hsrc[k], non_blocking=True)
-        run(dsets, ys[0], hs[0])
-        hy.copy_(ys[0], non_blocking=True)
-        hh.copy_(hs[0], non_blocking=True)
+    def upload(k, st):
+        for n in dsets[k]:
+            dsets[k][n].copy_(hsrc[n], non_blocking=True)
 
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.e2e_steps):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    def compute(k, st):
+        run(dsets[k], ys[k], hs[k], st=st, ut=utmp[k])
+
+    def download(k, st):
+        hy[k].copy_(ys[k], non_blocking=True)
+        hh[k].copy_(hs[k], non_blocking=True)
+
+    pipelined_e2e(torch, 3, upload, compute, download)   # warm-up
+    e2e_ms = pipelined_e2e(torch, args.e2e_steps, upload, compute, download)
     h2d = sum(v.numel() * v.element_size() for v in hsrc.values())
-    d2h = hy.numel() * hy.element_size() + hh.numel() * hh.element_size()
+    d2h = hy[0].numel() * hy[0].element_size() + hh[0].numel() * hh[0].element_size()
 
     peaks = measured_peaks()
     exps = Bsz * Dch * L * N
@@ -514,33 +551,30 @@ def bench_decode(args, m, torch):
         torch.cuda.synchronize()
     t_ms = ev0.elapsed_time(ev1) / args.steps
 
-    hst = states[0].cpu().pin_memory()
+    # end to end: every step uploads the state and the step's inputs from pinned host memory and downloads
+    # y and the new state; uploads and downloads overlap the neighbouring steps' kernels (two buffer sets)
+    hst = [states[k].cpu().pin_memory() for k in range(2)]
     hin = [{k: v.cpu().pin_memory() for k, v in s.items()} for s in steps_in[:2]]
-    hy = torch.empty((Bsz, Dch), dtype=torch.bfloat16).pin_memory()
-    dst = states[0]
-    dins = steps_in[0]
+    hy = [torch.empty((Bsz, Dch), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dins = [steps_in[0], steps_in[1]]
 
-    def e2e_step(i):
-        dst.copy_(hst, non_blocking=True)
-        for k in dins:
-            dins[k].copy_(hin[i % 2][k], non_blocking=True)
-        m.mamba_state_update(dst, dins["u"], dins["delta"], A, dins["B"], dins["C"], D, dins["z"], bias, 1, ys[0],
-                             stream=stream)
-        hy.copy_(ys[0], non_blocking=True)
-        hst.copy_(dst, non_blocking=True)
+    def upload(k, st):
+        states[k].copy_(hst[k], non_blocking=True)
+        for n in dins[k]:
+            dins[k][n].copy_(hin[k][n], non_blocking=True)
 
-    for i in range(3):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(args.e2e_steps):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    h2d = hst.numel() * 4 + sum(v.numel() * v.element_size() for v in hin[0].values())
-    d2h = hy.numel() * 2 + hst.numel() * 4
+    def compute(k, st):
+        m.mamba_state_update(states[k], dins[k]["u"], dins[k]["delta"], A, dins[k]["B"], dins[k]["C"], D,
+                             dins[k]["z"], bias, 1, ys[k], stream=st)
+
+    def download(k, st):
+        hy[k].copy_(ys[k], non_blocking=True)
+        hst[k].copy_(states[k], non_blocking=True)
+
+    pipelined_e2e(torch, 3, upload, compute, download)   # warm-up
+    e2e_ms = pipelined_e2e(torch, args.e2e_steps, upload, compute, download)
+    h2d = hst[0].numel() * 4 + sum(v.numel() * v.element_size() for v in hin[0].values())
+    d2h = hy[0].numel() * 2 + hst[0].numel() * 4
     peaks = measured_peaks()
     t_meas = t_ms * 1e-3
     roof = {"bound": "hbm", "achieved": round(nbytes / t_meas / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
