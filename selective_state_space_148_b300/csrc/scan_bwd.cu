@@ -49,24 +49,40 @@ struct BwdShape {
     static constexpr int S = 4, CH = 32, NTHR = S * CH;
     static constexpr int TC = 32 / NS;  // steps per chunk: TC * NS = 32 states kept per lane
     static constexpr int NP = S * NS;   // padded state count
-    // shared memory, floats: recomputed states [TC][NS][NTHR] and the dB, dC terms [TC][NS][NTHR] each;
-    // the chunk's inputs u, Delta_raw, z, dy [4][CH][TC] and B, C [2][TC][NP]; outputs du, ddelta, dz [3][CH][TC]
-    static constexpr int SH_FLOATS = TC * NS * NTHR;
+    // shared memory, floats: recomputed states [TC][NS][NTHR]; the dB, dC terms [TC][NP][CHP] each (channel
+    // innermost, padded to 33 so that the sum over channels reads distinct banks); the chunk's inputs u,
+    // Delta_raw, z, dy [4][CH][TC] and B, C [2][TC][NP]; outputs du, ddelta, dz [3][CH][TC]
+    static constexpr int CHP = CH + 1;
+    static constexpr int SH_FLOATS = TC * NS * NTHR, SD_FLOATS = TC * NP * CHP;
     static constexpr int IN_FLOATS = 4 * CH * TC, BC_FLOATS = 2 * TC * NP, OUT_FLOATS = 3 * CH * TC;
-    static constexpr size_t SMEM_BYTES = (3 * SH_FLOATS + IN_FLOATS + BC_FLOATS + OUT_FLOATS) * sizeof(float);
+    static constexpr size_t SMEM_BYTES =
+        (SH_FLOATS + 2 * SD_FLOATS + IN_FLOATS + BC_FLOATS + OUT_FLOATS) * sizeof(float);
 };
+
+// NS consecutive floats of shared memory (16-byte aligned) into registers with 16-byte loads
+template <int NS>
+__device__ __forceinline__ void load_vec(float (&v)[NS], const float *p) {
+#pragma unroll
+    for (int k = 0; k < NS; k += 4) {
+        const float4 q = *reinterpret_cast<const float4 *>(p + k);
+        v[k] = q.x;
+        v[k + 1] = q.y;
+        v[k + 2] = q.z;
+        v[k + 3] = q.w;
+    }
+}
 
 template <typename T, int NS>
 __global__ void __launch_bounds__(128)
 scan_bwd_kernel(const BwdArgs a, long long K) {
     using Sh = BwdShape<T, NS>;
     using IO = Io<T>;
-    constexpr int S = Sh::S, CH = Sh::CH, NTHR = Sh::NTHR, TC = Sh::TC, NP = Sh::NP;
+    constexpr int CH = Sh::CH, NTHR = Sh::NTHR, TC = Sh::TC, NP = Sh::NP;
     extern __shared__ float4 smem_f4[];
     float *const sH = reinterpret_cast<float *>(smem_f4);  // [TC][NS][NTHR]
-    float *const sdB = sH + Sh::SH_FLOATS;
-    float *const sdC = sdB + Sh::SH_FLOATS;
-    float *const sIn = sdC + Sh::SH_FLOATS;    // [4][CH][TC]: u, Delta_raw, z, dy
+    float *const sdB = sH + Sh::SH_FLOATS;     // [TC][NP][CHP]
+    float *const sdC = sdB + Sh::SD_FLOATS;
+    float *const sIn = sdC + Sh::SD_FLOATS;    // [4][CH][TC]: u, Delta_raw, z, dy
     float *const sBC = sIn + Sh::IN_FLOATS;    // [2][TC][NP]: B, C
     float *const sOut = sBC + Sh::BC_FLOATS;   // [3][CH][TC]: du, ddelta, dz
 
@@ -135,25 +151,60 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
     auto softplus_of = [&](float raw) { return a.softplus ? softplus_f(raw) : raw; };
 
     auto chunk_len = [&](long long k) { return (int)min((long long)TC, L - k * TC); };
-    // ---- forward sweep: checkpoint the state before every chunk
-    load_chunk(0, chunk_len(0), 2);
-    for (long long k = 0; k < K; ++k) {
-        const int nt = chunk_len(k);
+    // ---- forward sweep: checkpoint the state before every chunk.  It stages FW chunks (TW steps) of u,
+    // Delta_raw and B at a time, one window ahead, in the dB/dC scratch, which is idle until the reverse sweep.
+    constexpr int FW = 4, TW = FW * TC;
+    constexpr int FT = 2 * CH * TW / NTHR, FB = NP * TW / NTHR;  // elements per thread: u/Delta_raw, B
+    static_assert(2 * CH * TW == FT * NTHR && NP * TW == FB * NTHR, "window staging splits evenly");
+    static_assert(2 * CH * TW + NP * TW <= 2 * Sh::SD_FLOATS, "the window fits the dB/dC scratch");
+    float *const wIn = sdB;               // [2][CH][TW]: u, Delta_raw
+    float *const wB = sdB + 2 * CH * TW;  // [TW][NP]
+    float ft[FT], fb[FB];
+    auto load_window = [&](long long t0) {
 #pragma unroll
-        for (int j = 0; j < NS; ++j)
-            if (live[j]) ck[k * N + j] = h[j];
-        __syncthreads();
-        store_chunk();
-        __syncthreads();
-        if (k + 1 < K) load_chunk((k + 1) * TC, chunk_len(k + 1), 2);  // in flight during this chunk
+        for (int r = 0; r < FT; ++r) {
+            const int q = tid + r * NTHR;
+            const int tens = q / (CH * TW), cc = (q / TW) % CH, i = q % TW;
+            const long long dch = (long long)blockIdx.x * CH + cc;
+            ft[r] = (t0 + i < L && dch < a.Dch) ? IO::load(tens ? a.delta : a.u, (b * a.Dch + dch) * L + t0 + i) : 0.f;
+        }
 #pragma unroll
-        for (int i = 0; i < TC; ++i) {
-            if (i < nt) {
-                const float dl = softplus_of(in_r[i] + bias);
-                const float du = dl * in_u[i];
+        for (int r = 0; r < FB; ++r) {
+            const int q = tid + r * NTHR;
+            const int n = q / TW, i = q % TW;
+            fb[r] = (t0 + i < L && n < N) ? IO::load(a.Bm, bc0 + (long long)n * L + t0 + i) : 0.f;
+        }
+    };
+    auto store_window = [&]() {
+#pragma unroll
+        for (int r = 0; r < FT; ++r) wIn[tid + r * NTHR] = ft[r];
+#pragma unroll
+        for (int r = 0; r < FB; ++r) {
+            const int q = tid + r * NTHR;
+            wB[(q % TW) * NP + q / TW] = fb[r];
+        }
+    };
+    const long long nwin = (L + TW - 1) / TW;
+    load_window(0);
+    for (long long w = 0; w < nwin; ++w) {
+        __syncthreads();
+        store_window();
+        __syncthreads();
+        if (w + 1 < nwin) load_window((w + 1) * TW);  // in flight during this window
+#pragma unroll
+        for (int i = 0; i < TW; ++i) {
+            const long long t = w * TW + i;
+            if (t < L) {  // uniform
+                if (i % TC == 0) {
+#pragma unroll
+                    for (int j = 0; j < NS; ++j)
+                        if (live[j]) ck[(t / TC) * N + j] = h[j];
+                }
+                const float dl = softplus_of(wIn[(CH + c) * TW + i] + bias);
+                const float du = dl * wIn[c * TW + i];
 #pragma unroll
                 for (int j = 0; j < NS; ++j)
-                    h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * sBC[i * NP + s * NS + j]);
+                    h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * wB[i * NP + s * NS + j]);
             }
         }
     }
@@ -188,29 +239,38 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
                 const float dl = softplus_of(in_r[i] + bias);
                 dlr[i] = dl;
                 const float du = dl * in_u[i];
+                float Bv[NS];
+                load_vec<NS>(Bv, sBC + i * NP + s * NS);
 #pragma unroll
                 for (int j = 0; j < NS; ++j) {
-                    h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * sBC[i * NP + s * NS + j]);
+                    h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * Bv[j]);
                     sH[(i * NS + j) * NTHR + tid] = h[j];
                 }
             }
         }
+        float hcur[NS];  // h_t of the step being swept (h_{t-1} of the step after it)
+#pragma unroll
+        for (int j = 0; j < NS; ++j) hcur[j] = sH[((nt - 1) * NS + j) * NTHR + tid];
 #pragma unroll
         for (int i = TC - 1; i >= 0; --i) {
             if (i >= nt) continue;
             const float dl = dlr[i];
             const float raw = in_r[i] + bias;
             const float uu = in_u[i], dyt = in_dy[i];
-            const float *Bt = sBC + i * NP + s * NS, *Ct = sBC + (TC + i) * NP + s * NS;
+            float Bt[NS], Ct[NS], hprev[NS];
+            load_vec<NS>(Bt, sBC + i * NP + s * NS);
+            load_vec<NS>(Ct, sBC + (TC + i) * NP + s * NS);
+#pragma unroll
+            for (int j = 0; j < NS; ++j) hprev[j] = i > 0 ? sH[((i - 1) * NS + j) * NTHR + tid] : hstart[j];
             float g = 1.f, dzt = 0.f;
             if (has_z) {  // yhat = C . h_t + D u, the C . h part summed over the 4 lanes
                 float ch = 0.f;
 #pragma unroll
-                for (int j = 0; j < NS; ++j) ch = fmaf(Ct[j], sH[(i * NS + j) * NTHR + tid], ch);
+                for (int j = 0; j < NS; ++j) ch = fmaf(Ct[j], hcur[j], ch);
                 ch += __shfl_xor_sync(0xffffffffu, ch, 1);
                 ch += __shfl_xor_sync(0xffffffffu, ch, 2);
                 const float zt = in_z[i];
-                const float sg = 1.f / (1.f + __expf(-zt));
+                const float sg = rcp_approx(1.f + ex2_approx(-zt * kLog2e));
                 g = zt * sg;
                 dzt = dyt * fmaf(Dd, uu, ch) * sg * fmaf(zt, 1.f - sg, 1.f);
             }
@@ -218,13 +278,13 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
             float dup = 0.f, ddt = 0.f;
 #pragma unroll
             for (int j = 0; j < NS; ++j) {
-                const float ht = sH[(i * NS + j) * NTHR + tid];
-                const float hp = i > 0 ? sH[((i - 1) * NS + j) * NTHR + tid] : hstart[j];
-                sdC[(i * NS + j) * NTHR + tid] = dyh * ht;
+                const float ht = hcur[j], hp = hprev[j];
+                hcur[j] = hp;
+                sdC[(i * NP + s * NS + j) * Sh::CHP + c] = dyh * ht;
                 dh[j] = fmaf(dyh, Ct[j], dh[j]);
                 const float e = ex2_approx(dl * A2[j]);
-                sdB[(i * NS + j) * NTHR + tid] = dh[j] * dl * uu;
-                dup = fmaf(dh[j] * dl, Bt[j], dup);
+                sdB[(i * NP + s * NS + j) * Sh::CHP + c] = dh[j] * dl * uu;
+                dup = fmaf(dh[j] * dl, Bt[j], dup);  // (Bt, Ct from the chunk's B/C rows)
                 ddt = fmaf(dh[j], fmaf(Bt[j], uu, An[j] * e * hp), ddt);
                 dAacc[j] = fmaf(dh[j] * dl, e * hp, dAacc[j]);
                 dh[j] *= e;
@@ -234,7 +294,7 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
             ddt += __shfl_xor_sync(0xffffffffu, ddt, 1);
             ddt += __shfl_xor_sync(0xffffffffu, ddt, 2);
             if (s == 0) {
-                const float draw = a.softplus ? ddt / (1.f + __expf(-raw)) : ddt;
+                const float draw = a.softplus ? ddt * rcp_approx(1.f + ex2_approx(-raw * kLog2e)) : ddt;
                 sOut[c * TC + i] = fmaf(Dd, dyh, dup);
                 sOut[(CH + c) * TC + i] = draw;
                 sOut[(2 * CH + c) * TC + i] = dzt;
@@ -254,13 +314,14 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
                 IO::store(tens == 0 ? a.du : tens == 1 ? a.ddelta : a.dz, (b * a.Dch + dch) * L + t0 + i, sOut[q]);
         }
         for (int q = tid; q < nt * NP; q += NTHR) {
-            const int i = q / NP, n = q % NP;  // state n = s' * NS + j
-            const int sl = n / NS, j = n % NS;
+            const int i = q / NP, n = q % NP;
             if (n < N) {
+                const float *pb = sdB + (i * NP + n) * Sh::CHP, *pc = sdC + (i * NP + n) * Sh::CHP;
                 float sb = 0.f, sc = 0.f;
+#pragma unroll 8
                 for (int cc = 0; cc < CH; ++cc) {
-                    sb += sdB[(i * NS + j) * NTHR + cc * S + sl];
-                    sc += sdC[(i * NS + j) * NTHR + cc * S + sl];
+                    sb += pb[cc];
+                    sc += pc[cc];
                 }
                 atomicAdd(a.dB + bc0 + (long long)n * L + t0 + i, sb);
                 atomicAdd(a.dC + bc0 + (long long)n * L + t0 + i, sc);
