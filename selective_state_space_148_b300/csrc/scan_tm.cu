@@ -102,7 +102,7 @@ cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, int warps, long
     }
     const long long ch = 32LL * warps / S;
     dim3 grid((unsigned)((a.Dch + ch - 1) / ch), (unsigned)Bsz, (unsigned)grid_chunks);
-    kern<<<grid, 32 * warps, Sh::SMEM_BYTES, st>>>(a, maps);
+    kern<<<grid, 32 * (warps + 1), Sh::SMEM_BYTES, st>>>(a, maps);  // + the producer warp
     return cudaGetLastError();
 }
 

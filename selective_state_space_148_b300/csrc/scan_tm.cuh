@@ -29,16 +29,19 @@
 // TMEM columns.  A channel is spread over S = 4, 8 or 16 lanes (N <= 4 S), lane
 // m % S owning states 4(m % S)..+3 (warp w reads TMEM lanes 32(w % 4)..+31, and
 // the selector picks K row m % S, so a lane always receives its own 4 states'
-// B and C: 8 columns per step for every S).  A CTA of W warps (32 W / S
-// channels) takes the whole of TMEM (512 columns, one CTA per SM) as two
-// buffers of one 32-step super-tile each.  W (8..12) is chosen per problem so
-// that the CTAs fill the SMs in whole waves.  Per super-tile the CTA does,
-// once: one MMA (M=128, N=256, K=16), five tiled TMA loads (u, Delta_raw, z
-// boxes of 32 steps x 32 W / S channels, B and C boxes of 32 steps x 4 S
-// states; out-of-range rows and steps read as zero), one X build and one CTA
-// barrier.  The input ring has 3 stages, loaded two super-tiles ahead;
-// u/Delta_raw/z use the TMA's 16-byte-chunk swizzle so that the channels of a
-// warp hit distinct banks.
+// B and C: 8 columns per step for every S).  A CTA of W compute warps (32 W / S
+// channels) and one producer warp takes the whole of TMEM (512 columns, one
+// CTA per SM) as two buffers of one 32-step super-tile each.  W (8..11) is
+// chosen per problem so that the CTAs fill the SMs in whole waves.  Per
+// super-tile the producer warp does, once: five tiled TMA loads (u, Delta_raw,
+// z boxes of 32 steps x 32 W / S channels, B and C boxes of 32 steps x 4 S
+// states; out-of-range rows and steps read as zero), one X build and one MMA
+// (M=128, N=256, K=16).  The compute warps never wait for one another: each
+// waits for its super-tile's MMA (mbarrier full[buffer]) and, when done with
+// the buffer and its input stage, arrives on empty[buffer]; the producer waits
+// for all W arrivals before it rebuilds that buffer two super-tiles later.  The
+// input ring has 3 stages; u/Delta_raw/z use the TMA's 16-byte-chunk swizzle so
+// that the channels of a warp hit distinct banks.
 //
 // Per 8-step sub-tile i each lane loads its 64 TMEM columns, then in one
 // branch-free block computes Delta = softplus(.), Delta*u, D*u and SiLU(z) for
@@ -79,8 +82,9 @@ struct TmMaps {
 template <typename T, int MODE, int S_ = 4, bool CONV = false>
 struct TmShape {
     static constexpr int S = S_;
-    static constexpr int MIN_WARPS = 8, MAX_WARPS = 12;  // CTA width, 32 / S channels per warp
+    static constexpr int MIN_WARPS = 8, MAX_WARPS = 11;  // compute warps of a CTA, 32 / S channels each
     static constexpr int MAX_THR = 32 * MAX_WARPS, MAX_CH = MAX_THR / S;
+    static constexpr int LAUNCH_THR = MAX_THR + 32;       // + the producer warp
     static constexpr int TT = 32;                  // steps per super-tile
     static constexpr int TB = 8;                   // steps per sub-tile
     static constexpr int NSUB = TT / TB;
@@ -108,6 +112,7 @@ struct TmShape {
     static constexpr int OFF_P = OFF_DU + 2 * DU_BYTES;
     static constexpr int OFF_BAR = OFF_P + (MODE == MODE_FULL ? 2 * P_BYTES : 0);
     static constexpr int SMEM_BYTES = OFF_BAR + 128 + 1024;  // + room to align the base to 1024 bytes
+    static_assert(5 + NST <= 8, "full[2], empty[2], done and io[NST] in the first 64 bytes of the barrier block");
     static_assert(IO_TILE % 1024 == 0 && BC_TILE % 1024 == 0, "swizzled boxes need 1024-byte aligned tiles");
     static_assert(SWZ == 4 || SWZ == 8, "rows of 64 or 128 bytes");
     static_assert(S == 4 || S == 8 || S == 16, "4, 8 or 16 lanes per channel");
@@ -118,9 +123,9 @@ struct TmShape {
 // HAS_Z: the gate z is given (MODE_FULL only).  S lanes per channel.  CONV:
 // a.u holds x and u = SiLU(a.conv_b + causal width-4 conv with a.conv_w) is
 // formed here (ai.xwebgame.com summary, "running it in PyTorch" block).
-// blockDim.x = 32 W, W in 8..12.
+// blockDim.x = 32 (W + 1): W compute warps (8..11) and one producer warp.
 template <typename T, int MODE, bool HAS_Z, int S_, bool CONV = false>
-__global__ void __launch_bounds__(TmShape<T, MODE, S_, CONV>::MAX_THR, 1)
+__global__ void __launch_bounds__(TmShape<T, MODE, S_, CONV>::LAUNCH_THR, 1)
 scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     using Sh = TmShape<T, MODE, S_, CONV>;
     constexpr bool FAST = sizeof(T) == 2;
@@ -138,14 +143,15 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     float4 *const sDU = reinterpret_cast<float4 *>(smem + Sh::OFF_DU);  // [2][MAX_CH][4 pairs]
     float *const sP = reinterpret_cast<float *>(smem + Sh::OFF_P);      // [2][MAX_THR][P_STRIDE]
     uint64_t *const full = reinterpret_cast<uint64_t *>(smem + Sh::OFF_BAR);  // [2] MMA of a super-tile done
-    uint64_t *const xready = full + 2;                                        // X built by every warp
-    uint64_t *const done = full + 3;                                          // abort path: all MMAs done
-    uint64_t *const io = full + 4;                                            // [NST] stage loads landed
+    uint64_t *const empty = full + 2;  // [2] every compute warp is done with a super-tile's TMEM buffer and stage
+    uint64_t *const done = full + 4;   // abort path: all MMAs done
+    uint64_t *const io = full + 5;     // [NST] stage loads landed
     uint32_t *const taddr_s = reinterpret_cast<uint32_t *>(smem + Sh::OFF_BAR + 64);
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(smem + Sh::OFF_BAR + 68);
 
-    const int nthr = blockDim.x, ch = nthr / S;  // channels of this CTA
+    const int nthr = blockDim.x, ncw = nthr / 32 - 1, ch = 32 * ncw / S;  // compute warps, channels of this CTA
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool producer = warp == ncw;  // the last warp loads, builds X and issues the MMAs
     const int s = tid % S, c = tid / S;  // state slice, channel within the CTA
     // the 4 step pairs of a sub-tile: lane s handles pair ps for its channel's
     // Delta and y (lanes s >= 4 of a wider channel repeat lane s % 4's work and
@@ -154,7 +160,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     const bool pair_owner = s < 4;
     const long long d0 = (long long)blockIdx.x * ch;
     const long long d = d0 + c;
-    const bool valid = d < a.Dch;
+    const bool valid = !producer && d < a.Dch;
     const long long b = blockIdx.y;
     const int kch = blockIdx.z;
     const long long N = a.N, L = a.L;
@@ -181,7 +187,8 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     if (tid == 0) {
         tc::mbar_init(&full[0], 1);
         tc::mbar_init(&full[1], 1);
-        tc::mbar_init(xready, nthr / 32);
+        tc::mbar_init(&empty[0], ncw);
+        tc::mbar_init(&empty[1], ncw);
         tc::mbar_init(done, 1);
         for (int k = 0; k < NST; ++k) tc::mbar_init(&io[k], 1);
         *abort_flag = 0;
@@ -216,11 +223,14 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     // y of the step at offset r from t_begin in this lane's channel: ylane + r
     T *const ylane = reinterpret_cast<T *>(a.y) + ((b * a.Dch + dd) * L + t_begin);
 
-    // bounded wait that gives up at once when another warp has already given up
-    auto wait_or_abort = [&](uint64_t *bar, uint32_t parity) -> bool {
+    // bounded wait that gives up at once when another warp has already given up;
+    // the producer backs off between polls (its waits last up to a super-tile)
+    auto wait_or_abort = [&](uint64_t *bar, uint32_t parity, bool backoff) -> bool {
+        const uint32_t polls = backoff ? kWaitPolls / 8 : kWaitPolls;
         for (uint32_t it = 0;; ++it) {
             if (tc::mbar_test_wait(bar, parity)) return true;
-            if (*abort_flag != 0 || it >= kWaitPolls) return false;
+            if (*abort_flag != 0 || it >= polls) return false;
+            if (backoff) __nanosleep(32);
         }
     };
 
@@ -241,15 +251,14 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         tc::tma_load_3d(st + Sh::OFF_BC, &maps.B, x, 0, (int)b, bar);  // 4 S state rows, zero past N
         tc::tma_load_3d(st + Sh::OFF_BC + Sh::BC_TILE, &maps.C, x, 0, (int)b, bar);
     };
-    int last_loaded = -1;  // thread 0: latest super-tile whose loads were issued
 
     // X of one super-tile from its stage: column n = 16 * pair + j (column order
     // above), K row k = slice k's value (bf16), or K rows 3k..3k+2 its three
     // bf16 parts (fp32, S = 4)
-    auto x_build = [&](int xb, const unsigned char *st) {
+    auto x_build = [&](int xb, const unsigned char *st) {  // by the producer warp
         const T *raw = reinterpret_cast<const T *>(st + Sh::OFF_BC);  // [which][4 S][TT]
         unsigned char *xbase = sX + xb * Sh::X_BYTES;
-        for (int n = tid; n < COLS; n += nthr) {
+        for (int n = lane; n < COLS; n += 32) {
             const int j = n & 15;
             const int t = 2 * (n >> 4) + (j & 1);
             const int which = j >> 3, col = (j & 7) >> 1;
@@ -361,149 +370,153 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     };
 
     const uint64_t descA = tc::umma_desc(tc::smem_addr(sA), 128, 256);
-    auto issue_mma = [&](int sn) {  // thread 0: MMA of super-tile sn -> TMEM buffer sn & 1, completion on full[sn & 1]
+    auto issue_mma = [&](int sn) {  // producer lane 0: MMA of super-tile sn -> TMEM buffer sn & 1, completion on full[sn & 1]
         const uint32_t xaddr = tc::smem_addr(sX + (sn & 1) * Sh::X_BYTES);
         tc::fence_after_sync();
         tc::umma_bf16(*taddr_s + (sn & 1) * COLS, descA, tc::umma_desc(xaddr, 128, 256), kIdesc, 0u);
         tc::umma_commit(&full[sn & 1]);
     };
 
-    // ---- prologue: loads of super-tiles 0 and 1, X and MMA of super-tile 0, Delta of sub-tile 0
+    // ---- the producer warp runs ahead of the compute warps by up to two
+    // super-tiles (the two TMEM buffers): stage loads, X builds and MMAs.  The
+    // compute warps never wait for one another.
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
     const uint32_t tmem_lane = *taddr_s + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-    if (tid == 0) {
-        load_stage(0);
-        last_loaded = 0;
-        if (nsup > 1) {
-            load_stage(1);
-            last_loaded = 1;
-        }
-    }
-    if (!wait_or_abort(&io[0], 0)) *abort_flag = 1;
-    x_build(0, stage_of(0));
-    tc::fence_proxy_async();
-    __syncthreads();
-    int mma_issued = 0;  // thread 0
-    if (tid == 0 && *abort_flag == 0) {
-        issue_mma(0);
-        mma_issued = 1;
-    }
-    // (D u, SiLU z) of the step pairs whose y is still open, by sub-tile parity
-    float2 Du_r[2], g_r[2];
-    side_pair(stage_of(0), 0, 2 * ps, 0, Du_r[0], g_r[0]);
-    __syncwarp();
-
-    int k_cur = 0;  // stage of super-tile sup
-    for (int sup = 0; sup < nsup; ++sup) {
-        const int k_nxt = k_cur == NST - 1 ? 0 : k_cur + 1;
-        if (sup + 1 < nsup) {
-            // Every warp has finished super-tile sup - 1: TMEM buffer (sup + 1) & 1
-            // and X buffer (sup + 1) & 1 are free (their MMA was waited for), and
-            // so is the stage of sup - 1, which the loads of sup + 2 reuse.
-            tc::fence_before_sync();
-            __syncthreads();
-            tc::fence_after_sync();
-            if (tid == 0 && sup + 2 < nsup && *abort_flag == 0) {
-                load_stage(sup + 2);
-                last_loaded = sup + 2;
+    int last_loaded = -1;  // producer lane 0: latest super-tile whose loads were issued
+    int mma_issued = 0;    // producer lane 0: MMAs issued
+    if (producer) {
+        if (lane == 0)
+            for (int sn = 0; sn < NST && sn < nsup; ++sn) {
+                load_stage(sn);
+                last_loaded = sn;
             }
-            if (!wait_or_abort(&io[k_nxt], ((sup + 1) / NST) & 1)) *abort_flag = 1;
-            x_build((sup + 1) & 1, stage_of(k_nxt));
+        for (int sn = 0; sn < nsup; ++sn) {
+            // the stage of sn has landed; for sn >= 2 every compute warp is done
+            // with super-tile sn - 2, so TMEM buffer sn & 1, X buffer sn & 1 (its
+            // MMA was waited for) and the stage of sn - 2 are free
+            bool ok = __all_sync(0xffffffffu, wait_or_abort(&io[sn % NST], (sn / NST) & 1, true));
+            if (ok && sn >= 2)
+                ok = __all_sync(0xffffffffu, wait_or_abort(&empty[sn & 1], ((sn - 2) >> 1) & 1, true));
+            if (!ok) {
+                *abort_flag = 1;
+                break;
+            }
+            tc::fence_after_sync();
+            x_build(sn & 1, stage_of(sn % NST));
             tc::fence_proxy_async();
             __syncwarp();
-            tc::mbar_arrive_if(xready, lane == 0);
-            if (tid == 0) {
-                if (wait_or_abort(xready, sup & 1) && *abort_flag == 0) {
-                    issue_mma(sup + 1);
-                    mma_issued = sup + 2;
-                } else {
-                    *abort_flag = 1;
+            if (lane == 0) {
+                issue_mma(sn);
+                mma_issued = sn + 1;
+                const int m = sn + NST - 2;  // into the stage of super-tile sn - 2
+                if (sn >= 2 && m < nsup) {
+                    load_stage(m);
+                    last_loaded = m;
                 }
             }
+            __syncwarp();
         }
-        // this super-tile's B/C are in TMEM buffer sup & 1 (after an abort the
-        // loads below still read allocated TMEM; the results are then discarded)
-        if (!__all_sync(0xffffffffu, wait_or_abort(&full[sup & 1], (sup >> 1) & 1))) *abort_flag = 1;
-        tc::fence_after_sync();
-        const unsigned char *st_cur = stage_of(k_cur);
-        const unsigned char *st_nxt = stage_of(k_nxt);
-        const int r0 = sup * TT + 2 * ps;  // this lane's pair offset in sub-tile 0 of this super-tile
-#pragma unroll
-        for (int q = 0; q < NSUB; ++q) {
-            uint32_t bcu[2][32];
-            tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64, bcu[0]);
-            tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64 + 32, bcu[1]);
-            tc::tmem_wait_ld_tied(bcu[0], bcu[1]);
+    } else {
+        // (D u, SiLU z) of the step pairs whose y is still open, by sub-tile parity
+        float2 Du_r[2], g_r[2];
+        if (!__all_sync(0xffffffffu, wait_or_abort(&io[0], 0, false))) *abort_flag = 1;
+        side_pair(stage_of(0), 0, 2 * ps, 0, Du_r[0], g_r[0]);
+        __syncwarp();
 
-            // one block: y of sub-tile i-1, Delta etc. of sub-tile i+1, the
-            // recurrence of sub-tile i (i = 4 sup + q, so i & 1 == q & 1)
-            float4 dq[TB / 2];
+        int k_cur = 0;  // stage of super-tile sup
+        for (int sup = 0; sup < nsup; ++sup) {
+            const int k_nxt = k_cur == NST - 1 ? 0 : k_cur + 1;
+            // this super-tile's B/C are in TMEM buffer sup & 1 (after an abort the
+            // loads below still read allocated TMEM; the results are then discarded)
+            if (!__all_sync(0xffffffffu, wait_or_abort(&full[sup & 1], (sup >> 1) & 1, false))) *abort_flag = 1;
+            tc::fence_after_sync();
+            const unsigned char *st_cur = stage_of(k_cur);
+            const unsigned char *st_nxt = stage_of(k_nxt);
+            const int r0 = sup * TT + 2 * ps;  // this lane's pair offset in sub-tile 0 of this super-tile
 #pragma unroll
-            for (int p = 0; p < TB / 2; ++p) dq[p] = du_chan[(q & 1) * MAX_CH * 4 + p];
-            output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
-            if (q + 1 < NSUB)
-                side_pair(st_cur, q + 1, r0 + (q + 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
-            else
-                side_pair(st_nxt, 0, r0 + TT, 0, Du_r[0], g_r[0]);
-            float pq[TB];
+            for (int q = 0; q < NSUB; ++q) {
+                uint32_t bcu[2][32];
+                tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64, bcu[0]);
+                tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64 + 32, bcu[1]);
+                tc::tmem_wait_ld_tied(bcu[0], bcu[1]);
+
+                // one block: y of sub-tile i-1, Delta etc. of sub-tile i+1, the
+                // recurrence of sub-tile i (i = 4 sup + q, so i & 1 == q & 1)
+                float4 dq[TB / 2];
 #pragma unroll
-            for (int p = 0; p < TB / 2; ++p) {
-                const float2 dl = f2(dq[p].x, dq[p].y);
-                const float2 du = f2(dq[p].z, dq[p].w);
-                const uint32_t *bcp = bcu[p >> 1] + 16 * (p & 1);
+                for (int p = 0; p < TB / 2; ++p) dq[p] = du_chan[(q & 1) * MAX_CH * 4 + p];
+                output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+                if (q + 1 < NSUB) {
+                    side_pair(st_cur, q + 1, r0 + (q + 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+                } else {
+                    if (sup + 1 < nsup && !__all_sync(0xffffffffu, wait_or_abort(&io[k_nxt], ((sup + 1) / NST) & 1, false)))
+                        *abort_flag = 1;
+                    side_pair(st_nxt, 0, r0 + TT, 0, Du_r[0], g_r[0]);
+                }
+                float pq[TB];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 x = __fmul2_rn(dl, A2d[j]);
-                    const float2 bu = __fmul2_rn(du, f2(__uint_as_float(bcp[2 * j]), __uint_as_float(bcp[2 * j + 1])));
-                    hh[j].x = fmaf(ex2_approx(x.x), hh[j].y, bu.x);
-                    hh[j].y = fmaf(ex2_approx(x.y), hh[j].x, bu.y);
+                for (int p = 0; p < TB / 2; ++p) {
+                    const float2 dl = f2(dq[p].x, dq[p].y);
+                    const float2 du = f2(dq[p].z, dq[p].w);
+                    const uint32_t *bcp = bcu[p >> 1] + 16 * (p & 1);
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 x = __fmul2_rn(dl, A2d[j]);
+                        const float2 bu = __fmul2_rn(du, f2(__uint_as_float(bcp[2 * j]), __uint_as_float(bcp[2 * j + 1])));
+                        hh[j].x = fmaf(ex2_approx(x.x), hh[j].y, bu.x);
+                        hh[j].y = fmaf(ex2_approx(x.y), hh[j].x, bu.y);
+                    }
+                    if (MODE == MODE_FULL) {
+                        float2 P = __fmul2_rn(f2(__uint_as_float(bcp[8]), __uint_as_float(bcp[9])), hh[0]);
+                        P = __ffma2_rn(f2(__uint_as_float(bcp[10]), __uint_as_float(bcp[11])), hh[1], P);
+                        P = __ffma2_rn(f2(__uint_as_float(bcp[12]), __uint_as_float(bcp[13])), hh[2], P);
+                        P = __ffma2_rn(f2(__uint_as_float(bcp[14]), __uint_as_float(bcp[15])), hh[3], P);
+                        pq[2 * p] = P.x;
+                        pq[2 * p + 1] = P.y;
+                    }
                 }
                 if (MODE == MODE_FULL) {
-                    float2 P = __fmul2_rn(f2(__uint_as_float(bcp[8]), __uint_as_float(bcp[9])), hh[0]);
-                    P = __ffma2_rn(f2(__uint_as_float(bcp[10]), __uint_as_float(bcp[11])), hh[1], P);
-                    P = __ffma2_rn(f2(__uint_as_float(bcp[12]), __uint_as_float(bcp[13])), hh[2], P);
-                    P = __ffma2_rn(f2(__uint_as_float(bcp[14]), __uint_as_float(bcp[15])), hh[3], P);
-                    pq[2 * p] = P.x;
-                    pq[2 * p + 1] = P.y;
+                    float *prow = sP + ((q & 1) * Sh::MAX_THR + tid) * Sh::P_STRIDE;
+                    *reinterpret_cast<float4 *>(prow) = make_float4(pq[0], pq[1], pq[2], pq[3]);
+                    *reinterpret_cast<float4 *>(prow + 4) = make_float4(pq[4], pq[5], pq[6], pq[7]);
                 }
+                __syncwarp();  // partials of sub-tile i and Delta of sub-tile i+1 visible to the channel's lanes
             }
-            if (MODE == MODE_FULL) {
-                float *prow = sP + ((q & 1) * Sh::MAX_THR + tid) * Sh::P_STRIDE;
-                *reinterpret_cast<float4 *>(prow) = make_float4(pq[0], pq[1], pq[2], pq[3]);
-                *reinterpret_cast<float4 *>(prow + 4) = make_float4(pq[4], pq[5], pq[6], pq[7]);
-            }
-            __syncwarp();  // partials of sub-tile i and Delta of sub-tile i+1 visible to the channel's lanes
+            // this warp is done with TMEM buffer sup & 1 and with the stage of sup
+            tc::fence_before_sync();
+            __syncwarp();
+            tc::mbar_arrive_if(&empty[sup & 1], lane == 0);
+            k_cur = k_nxt;
         }
-        k_cur = k_nxt;
-    }
 
-    output_pair((nsup - 1) * TT + 3 * TB + 2 * ps, 1, Du_r[1], g_r[1]);  // the last sub-tile is odd
-    if (MODE == MODE_STATES) {
-        float sdt = sdt_acc;
+        output_pair((nsup - 1) * TT + 3 * TB + 2 * ps, 1, Du_r[1], g_r[1]);  // the last sub-tile is odd
+        if (MODE == MODE_STATES) {
+            float sdt = sdt_acc;
 #pragma unroll
-        for (int off = 1; off < S; off <<= 1) sdt += __shfl_xor_sync(0xffffffffu, sdt, off);
-        if (valid) {
-            const long long base = (b * a.nchunks + kch) * a.Dch + d;
+            for (int off = 1; off < S; off <<= 1) sdt += __shfl_xor_sync(0xffffffffu, sdt, off);
+            if (valid) {
+                const long long base = (b * a.nchunks + kch) * a.Dch + d;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const long long n = 4LL * s + j;
+                    if (n < N) a.ws_h[base * N + n] = hh[j].y;
+                }
+                if (s == 0) a.ws_sdt[base] = sdt;
+            }
+        } else if (a.last_state != nullptr && valid && kch == a.nchunks - 1) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const long long n = 4LL * s + j;
-                if (n < N) a.ws_h[base * N + n] = hh[j].y;
+                if (n < N) a.last_state[(b * a.Dch + d) * N + n] = hh[j].y;
             }
-            if (s == 0) a.ws_sdt[base] = sdt;
-        }
-    } else if (a.last_state != nullptr && valid && kch == a.nchunks - 1) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const long long n = 4LL * s + j;
-            if (n < N) a.last_state[(b * a.Dch + d) * N + n] = hh[j].y;
         }
     }
 
     tc::fence_before_sync();
     __syncthreads();
-    if (tid == 0 && *abort_flag != 0) {
+    if (producer && lane == 0 && *abort_flag != 0) {
         atomicOr(&g_device_error, 1u);
         // the MMAs and loads this CTA started must finish before its TMEM and
         // shared memory are released (each stage has at most its latest
