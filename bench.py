@@ -347,7 +347,7 @@ def aggregate_gbs(world, bytes_per_rank_step, t_ms, e2e_ms):
     return (world * bytes_per_rank_step / (t_ms * 1e-3) / 1e9, world * bytes_per_rank_step / (e2e_ms * 1e-3) / 1e9)
 
 
-def traffic_record(kernel_key):
+def traffic_record(kernel_key, sources=None):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
@@ -355,20 +355,21 @@ def traffic_record(kernel_key):
     rec = json.load(open(p)).get(kernel_key)
     if not rec:
         return None
-    if rec.get("source_sha") != kernel_source_sha():
+    if rec.get("source_sha") != kernel_source_sha(sources or SCAN_KERNEL_SOURCES):
         return None
     return rec.get("dram_bytes_per_launch")
 
 
-# the sources the forward scan kernels are built from (a change to any of them voids a stored ncu record)
+# the sources a kernel is built from (a change to any of them voids its stored ncu record)
 SCAN_KERNEL_SOURCES = ("scan_tm.cuh", "scan_tm.cu", "tcgen05.cuh", "common.cuh", "scan_kernels.cuh", "scan_fwd.cu",
                        "internal.h")
+DECODE_KERNEL_SOURCES = ("state_update.cu", "common.cuh", "internal.h")
 
 
-def kernel_source_sha():
+def kernel_source_sha(sources=SCAN_KERNEL_SOURCES):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_148_b300", "csrc")
-    for f in SCAN_KERNEL_SOURCES:
+    for f in sources:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -579,7 +580,7 @@ def bench_decode(args, m, torch):
     t_meas = t_ms * 1e-3
     roof = {"bound": "hbm", "achieved": round(nbytes / t_meas / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(nbytes / (peaks["hbm_gbs"] * 1e9) / t_meas, 4),
-            "traffic": traffic_record(cfg["name"]), "kernel": "state_update_rows_kernel<bf16,NP16,1>",
+            "traffic": traffic_record(cfg["name"], DECODE_KERNEL_SOURCES), "kernel": "state_update_rows_kernel<bf16,NP16,R1,V8>",
             "peak_source": f"{peaks['source']} copy bandwidth"}
     return dict(ms_per_step=t_ms, bytes=nbytes, tokens=Bsz, dtype="bf16",
                 config={"workload": cfg["name"], "batch": Bsz, "d_inner": Dch, "d_state": N, "io": io,

@@ -256,8 +256,17 @@ int mamba_state_update(float *state, const void *u, const void *delta, const flo
     a.Dch = Dch;
     a.N = N;
     a.softplus = softplus_flag ? 1 : 0;
-    const bool vec = (N % 4 == 0) && aligned16(state) && aligned16(A) && Bsz * Dch < (1LL << 31);
-    return launch_state_update(dtype, vec, a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+    // the aligned kernel reads V = 8 or 4 consecutive states of state, A, B and C per lane with
+    // 16-byte (and, for bf16 B/C with V = 4, 8-byte) loads
+    auto aligned_to = [](const void *p, uintptr_t bytes) { return (reinterpret_cast<uintptr_t>(p) & (bytes - 1u)) == 0; };
+    const uintptr_t eb = (uintptr_t)io_bytes(dtype);
+    const bool rows_ok = aligned16(state) && aligned16(A) && Bsz * Dch < (1LL << 31);
+    int lane_states = 0;
+    if (rows_ok && N % 8 == 0 && aligned_to(B, 8 * eb) && aligned_to(C, 8 * eb))
+        lane_states = 8;
+    else if (rows_ok && N % 4 == 0 && aligned_to(B, 4 * eb) && aligned_to(C, 4 * eb))
+        lane_states = 4;
+    return launch_state_update(dtype, lane_states, a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? MAMBA_OK
                : MAMBA_ERR_LAUNCH;
 }

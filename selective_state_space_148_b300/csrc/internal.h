@@ -45,7 +45,9 @@ struct StepArgs {
     long long Bsz, Dch, N;
     int softplus;
 };
-cudaError_t launch_state_update(int dtype, bool vec, const StepArgs &a, cudaStream_t st);
+// lane_states: 8 or 4 for the aligned kernel with that many states per lane (16-byte aligned
+// state and A rows, N and the B/C alignment multiples of it), 0 for the scalar kernel.
+cudaError_t launch_state_update(int dtype, int lane_states, const StepArgs &a, cudaStream_t st);
 
 // Depthwise causal conv (width 4) + optional SiLU over rows of length L
 // (row r uses taps w[r % Dch]); vec: 16-byte aligned x, u, w and 16-byte rows.
