@@ -121,19 +121,23 @@ class ClockSampler:
             self.nvml = None
             self.error = str(e)
 
+    def _sample(self):
+        c = self.nvml.sm_clock()
+        if c is not None:
+            self.samples.append(c)
+        r = self.nvml.reasons()
+        for bit, name in self.REASONS.items():
+            if r & bit:
+                self.reasons.add(name)
+
     def _run(self):
         while not self._stop.is_set():
-            c = self.nvml.sm_clock()
-            if c is not None:
-                self.samples.append(c)
-            r = self.nvml.reasons()
-            for bit, name in self.REASONS.items():
-                if r & bit:
-                    self.reasons.add(name)
+            self._sample()
             time.sleep(0.001)
 
     def __enter__(self):
         if self.nvml is not None:
+            self._sample()  # at least one sample at each end of a short timed region
             self._t = threading.Thread(target=self._run, daemon=True)
             self._t.start()
         return self
@@ -142,6 +146,7 @@ class ClockSampler:
         self._stop.set()
         if self._t is not None:
             self._t.join()
+            self._sample()
 
     def summary(self):
         out = {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
