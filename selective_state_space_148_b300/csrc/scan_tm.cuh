@@ -352,14 +352,19 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
             if (HAS_Z) g = silu2<FAST>(unpack(stage_word(st, 2, q)));
         }
     };
-    const float *const p_chan = sP + (c * S) * Sh::P_STRIDE + 2 * ps;  // + (i & 1) * MAX_THR * P_STRIDE
-    // y of this lane's pair at offset r from the channel's 4 partial sums
+    // partial sums of this lane's group of 4 lanes (lanes 4 (s / 4) .. + 3 of the channel)
+    const float *const p_chan = sP + (c * S + (s & ~3)) * Sh::P_STRIDE + 2 * ps;  // + (i & 1) * MAX_THR * P_STRIDE
+    // y of this lane's pair at offset r from the channel's S partial sums: each lane adds its group's
+    // 4 partials, the S / 4 groups are combined with shuffles
     auto output_pair = [&](int r, int par, float2 Du, float2 g) {
         if (MODE != MODE_FULL) return;
         const float *pp = p_chan + par * Sh::MAX_THR * Sh::P_STRIDE;
         float2 ys = *reinterpret_cast<const float2 *>(pp);
 #pragma unroll
-        for (int k = 1; k < S; ++k) ys = __fadd2_rn(ys, *reinterpret_cast<const float2 *>(pp + k * Sh::P_STRIDE));
+        for (int k = 1; k < 4; ++k) ys = __fadd2_rn(ys, *reinterpret_cast<const float2 *>(pp + k * Sh::P_STRIDE));
+#pragma unroll
+        for (int off = 4; off < S; off <<= 1)
+            ys = __fadd2_rn(ys, f2(__shfl_xor_sync(0xffffffffu, ys.x, off), __shfl_xor_sync(0xffffffffu, ys.y, off)));
         float2 yy = __fadd2_rn(ys, Du);
         if (HAS_Z) yy = __fmul2_rn(yy, g);
         const bool st = pair_owner && (unsigned)r < lenv;
