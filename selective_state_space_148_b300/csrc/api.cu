@@ -1,6 +1,7 @@
 // api.cu -- the C ABI (include/mamba_scan.h): argument validation, choice
 // between the direct and the chunked scan, stream-ordered workspace, and
 // mapping of CUDA errors to status codes.  No C++ exception leaves this file.
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -68,7 +69,7 @@ struct Plan {
     int K;
 };
 
-int make_plan(long long Bsz, long long Dch, long long L, long long N, long long chunk_len_req, Plan *plan) {
+int make_plan(long long Bsz, long long Dch, long long L, long long N, int dtype, long long chunk_len_req, Plan *plan) {
     const ScanGeom g = scan_geom(N);
     if (chunk_len_req < 0) {
         *plan = Plan{L, 1};
@@ -85,6 +86,33 @@ int make_plan(long long Bsz, long long Dch, long long L, long long N, long long 
         int sms = 0;
         const int st = sm_count(&sms);
         if (st != MAMBA_OK) return st;
+        if (tm_kernel_for(dtype, N) && L >= 16LL * g.TT) {
+            // The tensor-memory kernel runs one CTA per SM: a launch costs whole waves.  The chunked
+            // scan runs K - 1 chunks (end states) and then K chunks (outputs), each pass costing its
+            // waves times the chunk length; take the K (narrower chunks only when strictly cheaper)
+            // that minimises (cost(K - 1) + cost(K)) * chunk_len, against cost(1) * L for the direct scan.
+            const int S = N <= 16 ? 4 : N <= 32 ? 8 : 16;
+            double best = (double)tm_launch_cost(Bsz, Dch, 1, sms, S, nullptr) * (double)L;
+            long long best_cl = L;
+            const long long kmax = std::min<long long>(L / (8LL * g.TT), 1024);  // chunks of at least 8 tiles
+            for (long long K = 2; K <= kmax; ++K) {
+                const long long c = ((L + K - 1) / K + g.TT - 1) / g.TT * g.TT;
+                const long long Kr = (L + c - 1) / c;
+                if (Kr < 2) continue;
+                const double t = (double)(tm_launch_cost(Bsz, Dch, (int)(Kr - 1), sms, S, nullptr) +
+                                          tm_launch_cost(Bsz, Dch, (int)Kr, sms, S, nullptr)) * (double)c;
+                if (t < best * (1.0 - 1e-9)) {
+                    best = t;
+                    best_cl = c;
+                }
+            }
+            if (best_cl >= L) {
+                *plan = Plan{L, 1};
+                return MAMBA_OK;
+            }
+            *plan = Plan{best_cl, (int)((L + best_cl - 1) / best_cl)};
+            return MAMBA_OK;
+        }
         const long long lanes = Bsz * Dch * g.S;
         const long long target = (long long)sms * 1024;  // lanes the GPU can keep in flight
         if (lanes * 4 >= target || L < 16LL * g.TT) {
@@ -129,7 +157,7 @@ int scan_impl(const void *u, const void *delta, const float *A, const void *B, c
     if (flags & ~(MAMBA_FLAG_ZOH | MAMBA_FLAG_REVERSE)) return MAMBA_ERR_BAD_FLAGS;
 
     Plan plan;
-    st = make_plan(Bsz, Dch, L, N, chunk_len, &plan);
+    st = make_plan(Bsz, Dch, L, N, dtype, chunk_len, &plan);
     if (st != MAMBA_OK) return st;
 
     const bool vec = aligned16(u) && aligned16(delta) && aligned16(B) && aligned16(C) && aligned16(y) &&
@@ -231,7 +259,7 @@ int mamba_selective_scan_fwd_ex(const void *u, const void *delta, const float *A
 size_t mamba_scan_workspace_size(int64_t Bsz, int64_t Dch, int64_t L, int64_t N, int64_t chunk_len, int dtype) {
     if (check_sizes(Bsz, Dch, L, N, dtype) != MAMBA_OK) return (size_t)-1;
     Plan plan;
-    if (make_plan(Bsz, Dch, L, N, chunk_len, &plan) != MAMBA_OK) return (size_t)-1;
+    if (make_plan(Bsz, Dch, L, N, dtype, chunk_len, &plan) != MAMBA_OK) return (size_t)-1;
     return workspace_bytes_for(Bsz, Dch, N, plan.K);
 }
 

@@ -21,6 +21,16 @@ struct ScanGeom {
 };
 ScanGeom scan_geom(long long N);
 
+// Cost of one launch of the tensor-memory scan kernel in units of one CTA's time: waves of CTAs (one
+// CTA per SM) times the warps of the busiest SM sub-partition (W compute warps and the producer warp
+// over 4 sub-partitions set the pace of a CTA).  *warps (if not null) receives the width W that
+// minimises it, the narrower one on ties.  S = lanes per channel (4, 8 or 16).
+long long tm_launch_cost(long long Bsz, long long Dch, int grid_chunks, int sms, int S, int *warps);
+
+// Whether the tensor-memory kernel is the one that serves problems of this storage type and state
+// count (on 16-byte aligned data without flags).
+bool tm_kernel_for(int dtype, long long N);
+
 // Launch the scan kernel: grid (ceil(Dch/CH), Bsz, grid_chunks).
 cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long long Bsz, int grid_chunks,
                         cudaStream_t st);

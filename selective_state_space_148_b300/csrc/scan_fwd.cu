@@ -87,6 +87,8 @@ static bool use_tmem_kernel() {
     return choice != 0;
 }
 
+bool tm_kernel_for(int dtype, long long N) { return N > 8 && N <= 64 && (dtype == 1 || N <= 16) && use_tmem_kernel(); }
+
 cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long long Bsz, int grid_chunks,
                         cudaStream_t st) {
     // the convolution-fed scan exists only in the tensor-memory kernel: never

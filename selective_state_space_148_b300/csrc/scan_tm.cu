@@ -14,6 +14,24 @@ __device__ unsigned int g_device_error = 0;
 
 namespace mamba {
 
+long long tm_launch_cost(long long Bsz, long long Dch, int grid_chunks, int sms, int S, int *warps) {
+    using Sh = TmShape<float, MODE_FULL>;
+    int best = Sh::MAX_WARPS;
+    long long best_cost = -1;
+    for (int w = Sh::MIN_WARPS; w <= Sh::MAX_WARPS; ++w) {
+        const long long cw = 32LL * w / S;  // channels per CTA
+        const long long ctas = Bsz * ((Dch + cw - 1) / cw) * grid_chunks;
+        const long long waves = sms > 0 ? (ctas + sms - 1) / sms : 1;
+        const long long cost = waves * ((w + 1 + 3) / 4);  // + the producer warp, over 4 sub-partitions
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = w;
+        }
+    }
+    if (warps != nullptr) *warps = best;
+    return best_cost;
+}
+
 namespace {
 
 // cuTensorMapEncodeTiled, reached through the runtime's driver entry point so
@@ -66,24 +84,11 @@ int device_sms() {
     return cache[dev];
 }
 
-// CTA width in warps (32 / S channels each).  One CTA runs per SM, so the
-// time is set by the number of waves times the work of one CTA; pick the width
-// that minimises waves x warps (wider on ties).
+// CTA width in warps (32 / S channels each): the one tm_launch_cost picks.
 int choose_warps(long long Bsz, long long Dch, int grid_chunks, int sms, int S) {
-    using Sh = TmShape<float, MODE_FULL>;
-    int best = Sh::MAX_WARPS;
-    long long best_cost = -1;
-    for (int w = Sh::MAX_WARPS; w >= Sh::MIN_WARPS; --w) {
-        const long long cw = 32LL * w / S;  // channels per CTA
-        const long long ctas = Bsz * ((Dch + cw - 1) / cw) * grid_chunks;
-        const long long waves = sms > 0 ? (ctas + sms - 1) / sms : 1;
-        const long long cost = waves * w;
-        if (best_cost < 0 || cost < best_cost) {
-            best_cost = cost;
-            best = w;
-        }
-    }
-    return best;
+    int w = 0;
+    tm_launch_cost(Bsz, Dch, grid_chunks, sms, S, &w);
+    return w;
 }
 
 template <typename T, int MODE, bool HAS_Z, int S, bool CONV = false>
