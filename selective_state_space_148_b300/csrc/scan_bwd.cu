@@ -28,6 +28,7 @@
 // the end.  No device-side waits.
 #include <cstdlib>
 #include <cstring>
+#include <type_traits>
 
 #include "../../include/mamba_scan.h"
 #include "internal.h"
@@ -50,11 +51,15 @@ struct BwdShape {
     static constexpr int TC = 32 / NS;  // steps per chunk: TC * NS = 32 states kept per lane
     static constexpr int NP = S * NS;   // padded state count
     // shared memory, floats: recomputed states [TC][NS][NTHR]; the dB, dC terms [TC][NP][CHP] each (channel
-    // innermost, padded to 33 so that the sum over channels reads distinct banks); the chunk's inputs u,
-    // Delta_raw, z, dy [4][CH][TC] and B, C [2][TC][NP]; outputs du, ddelta, dz [3][CH][TC]
-    static constexpr int CHP = CH + 1;
+    // innermost, padded to 33 so that the sum over channels reads distinct banks; a term of channel c and
+    // state slice s goes to column (c + ROT s) mod 32, which puts the 32 lanes of a warp's store in 32
+    // banks, and the sum over a row does not depend on the column order); the chunk's inputs u, Delta_raw,
+    // z, dy [4][CH][TCP] and B, C [2][TC][NP]; outputs du, ddelta, dz [3][CH][TCP] (rows padded to TCP =
+    // TC + 1 so that the 8 channels of a warp read distinct banks)
+    static constexpr int CHP = CH + 1, TCP = TC + 1, ROT = (8 - NS) & 31;
     static constexpr int SH_FLOATS = TC * NS * NTHR, SD_FLOATS = TC * NP * CHP;
-    static constexpr int IN_FLOATS = 4 * CH * TC, BC_FLOATS = 2 * TC * NP, OUT_FLOATS = 3 * CH * TC;
+    static constexpr int IN_FLOATS = 4 * CH * TCP, BC_FLOATS = 2 * TC * NP, OUT_FLOATS = 3 * CH * TCP;
+    static_assert(CH == 32, "the column rotation permutes 32 channels");
     static constexpr size_t SMEM_BYTES =
         (SH_FLOATS + 2 * SD_FLOATS + IN_FLOATS + BC_FLOATS + OUT_FLOATS) * sizeof(float);
 };
@@ -108,8 +113,10 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
     const float Dd = (a.D != nullptr && valid) ? a.D[dd] : 0.f;
     const float bias = (a.bias != nullptr && valid) ? a.bias[dd] : 0.f;
     float *const ck = a.ckpt + ((b * a.Dch + dd) * K) * N + (long long)s * NS;
-    const float *const in_u = sIn + c * TC, *const in_r = sIn + (CH + c) * TC;
-    const float *const in_z = sIn + (2 * CH + c) * TC, *const in_dy = sIn + (3 * CH + c) * TC;
+    constexpr int TCP = Sh::TCP;
+    const float *const in_u = sIn + c * TCP, *const in_r = sIn + (CH + c) * TCP;
+    const float *const in_z = sIn + (2 * CH + c) * TCP, *const in_dy = sIn + (3 * CH + c) * TCP;
+    const int dcol = (c + Sh::ROT * s) & 31;  // this lane's column in the dB/dC term rows
 
     // Inputs of steps t0 .. t0 + nt - 1 (zero past the end, past Dch, past N): loaded into registers one
     // chunk ahead (load_chunk), written to shared memory when the chunk starts (store_chunk).  ntens = 2: u
@@ -140,7 +147,10 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
     };
     auto store_chunk = [&]() {
 #pragma unroll
-        for (int r = 0; r < PT; ++r) sIn[tid + r * NTHR] = pt[r];
+        for (int r = 0; r < PT; ++r) {
+            const int q = tid + r * NTHR;  // (tensor, channel) row q / TC, step q % TC
+            sIn[(q / TC) * TCP + q % TC] = pt[r];
+        }
 #pragma unroll
         for (int r = 0; r < PB; ++r) {
             const int q = tid + r * NTHR;
@@ -156,9 +166,10 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
     constexpr int FW = 4, TW = FW * TC;
     constexpr int FT = 2 * CH * TW / NTHR, FB = NP * TW / NTHR;  // elements per thread: u/Delta_raw, B
     static_assert(2 * CH * TW == FT * NTHR && NP * TW == FB * NTHR, "window staging splits evenly");
-    static_assert(2 * CH * TW + NP * TW <= 2 * Sh::SD_FLOATS, "the window fits the dB/dC scratch");
-    float *const wIn = sdB;               // [2][CH][TW]: u, Delta_raw
-    float *const wB = sdB + 2 * CH * TW;  // [TW][NP]
+    constexpr int TWP = TW + 1;  // padded rows: the 8 channels of a warp read distinct banks
+    static_assert(2 * CH * TWP + NP * TW <= 2 * Sh::SD_FLOATS, "the window fits the dB/dC scratch");
+    float *const wIn = sdB;                // [2][CH][TWP]: u, Delta_raw
+    float *const wB = sdB + 2 * CH * TWP;  // [TW][NP]
     float ft[FT], fb[FB];
     auto load_window = [&](long long t0) {
 #pragma unroll
@@ -177,7 +188,10 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
     };
     auto store_window = [&]() {
 #pragma unroll
-        for (int r = 0; r < FT; ++r) wIn[tid + r * NTHR] = ft[r];
+        for (int r = 0; r < FT; ++r) {
+            const int q = tid + r * NTHR;
+            wIn[(q / TW) * TWP + q % TW] = ft[r];
+        }
 #pragma unroll
         for (int r = 0; r < FB; ++r) {
             const int q = tid + r * NTHR;
@@ -200,8 +214,8 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
                     for (int j = 0; j < NS; ++j)
                         if (live[j]) ck[(t / TC) * N + j] = h[j];
                 }
-                const float dl = softplus_of(wIn[(CH + c) * TW + i] + bias);
-                const float du = dl * wIn[c * TW + i];
+                const float dl = softplus_of(wIn[(CH + c) * TWP + i] + bias);
+                const float du = dl * wIn[c * TWP + i];
 #pragma unroll
                 for (int j = 0; j < NS; ++j)
                     h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * wB[i * NP + s * NS + j]);
@@ -232,78 +246,86 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
 #pragma unroll
             for (int j = 0; j < NS; ++j) hnext[j] = live[j] ? ck[(k - 1) * N + j] : 0.f;
         }
+        // the chunk body, without per-step length tests for whole chunks (all but possibly the last)
+        auto sweep = [&](auto full_tag) {
+            constexpr bool FULLC = decltype(full_tag)::value;
 #pragma unroll
-        for (int i = 0; i < TC; ++i) {  // recompute the chunk's states (private to this lane)
-            dlr[i] = 0.f;
-            if (i < nt) {
-                const float dl = softplus_of(in_r[i] + bias);
-                dlr[i] = dl;
-                const float du = dl * in_u[i];
-                float Bv[NS];
-                load_vec<NS>(Bv, sBC + i * NP + s * NS);
+            for (int i = 0; i < TC; ++i) {  // recompute the chunk's states (private to this lane)
+                dlr[i] = 0.f;
+                if (FULLC || i < nt) {
+                    const float dl = softplus_of(in_r[i] + bias);
+                    dlr[i] = dl;
+                    const float du = dl * in_u[i];
+                    float Bv[NS];
+                    load_vec<NS>(Bv, sBC + i * NP + s * NS);
+#pragma unroll
+                    for (int j = 0; j < NS; ++j) {
+                        h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * Bv[j]);
+                        sH[(i * NS + j) * NTHR + tid] = h[j];
+                    }
+                }
+            }
+            float hcur[NS];  // h_t of the step being swept (h_{t-1} of the step after it)
+#pragma unroll
+            for (int j = 0; j < NS; ++j) hcur[j] = sH[((FULLC ? TC - 1 : nt - 1) * NS + j) * NTHR + tid];
+#pragma unroll
+            for (int i = TC - 1; i >= 0; --i) {
+                if (!FULLC && i >= nt) continue;
+                const float dl = dlr[i];
+                const float raw = in_r[i] + bias;
+                const float uu = in_u[i], dyt = in_dy[i];
+                float Bt[NS], Ct[NS], hprev[NS];
+                load_vec<NS>(Bt, sBC + i * NP + s * NS);
+                load_vec<NS>(Ct, sBC + (TC + i) * NP + s * NS);
+#pragma unroll
+                for (int j = 0; j < NS; ++j) hprev[j] = i > 0 ? sH[((i - 1) * NS + j) * NTHR + tid] : hstart[j];
+                float g = 1.f, dzt = 0.f;
+                if (has_z) {  // yhat = C . h_t + D u, the C . h part summed over the 4 lanes
+                    float ch = 0.f;
+#pragma unroll
+                    for (int j = 0; j < NS; ++j) ch = fmaf(Ct[j], hcur[j], ch);
+                    ch += __shfl_xor_sync(0xffffffffu, ch, 1);
+                    ch += __shfl_xor_sync(0xffffffffu, ch, 2);
+                    const float zt = in_z[i];
+                    const float sg = rcp_approx(1.f + ex2_approx(-zt * kLog2e));
+                    g = zt * sg;
+                    dzt = dyt * fmaf(Dd, uu, ch) * sg * fmaf(zt, 1.f - sg, 1.f);
+                }
+                const float dyh = dyt * g;
+                float dup = 0.f, ddt = 0.f;
 #pragma unroll
                 for (int j = 0; j < NS; ++j) {
-                    h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * Bv[j]);
-                    sH[(i * NS + j) * NTHR + tid] = h[j];
+                    const float ht = hcur[j], hp = hprev[j];
+                    hcur[j] = hp;
+                    sdC[(i * NP + s * NS + j) * Sh::CHP + dcol] = dyh * ht;
+                    dh[j] = fmaf(dyh, Ct[j], dh[j]);
+                    const float e = ex2_approx(dl * A2[j]);
+                    sdB[(i * NP + s * NS + j) * Sh::CHP + dcol] = dh[j] * dl * uu;
+                    dup = fmaf(dh[j] * dl, Bt[j], dup);  // (Bt, Ct from the chunk's B/C rows)
+                    ddt = fmaf(dh[j], fmaf(Bt[j], uu, An[j] * e * hp), ddt);
+                    dAacc[j] = fmaf(dh[j] * dl, e * hp, dAacc[j]);
+                    dh[j] *= e;
+                }
+                dup += __shfl_xor_sync(0xffffffffu, dup, 1);
+                dup += __shfl_xor_sync(0xffffffffu, dup, 2);
+                ddt += __shfl_xor_sync(0xffffffffu, ddt, 1);
+                ddt += __shfl_xor_sync(0xffffffffu, ddt, 2);
+                if (s == 0) {
+                    const float draw = a.softplus ? ddt * rcp_approx(1.f + ex2_approx(-raw * kLog2e)) : ddt;
+                    sOut[c * TCP + i] = fmaf(Dd, dyh, dup);
+                    sOut[(CH + c) * TCP + i] = draw;
+                    sOut[(2 * CH + c) * TCP + i] = dzt;
+                    if (valid) {
+                        dDacc = fmaf(dyh, uu, dDacc);
+                        dbacc += draw;
+                    }
                 }
             }
-        }
-        float hcur[NS];  // h_t of the step being swept (h_{t-1} of the step after it)
-#pragma unroll
-        for (int j = 0; j < NS; ++j) hcur[j] = sH[((nt - 1) * NS + j) * NTHR + tid];
-#pragma unroll
-        for (int i = TC - 1; i >= 0; --i) {
-            if (i >= nt) continue;
-            const float dl = dlr[i];
-            const float raw = in_r[i] + bias;
-            const float uu = in_u[i], dyt = in_dy[i];
-            float Bt[NS], Ct[NS], hprev[NS];
-            load_vec<NS>(Bt, sBC + i * NP + s * NS);
-            load_vec<NS>(Ct, sBC + (TC + i) * NP + s * NS);
-#pragma unroll
-            for (int j = 0; j < NS; ++j) hprev[j] = i > 0 ? sH[((i - 1) * NS + j) * NTHR + tid] : hstart[j];
-            float g = 1.f, dzt = 0.f;
-            if (has_z) {  // yhat = C . h_t + D u, the C . h part summed over the 4 lanes
-                float ch = 0.f;
-#pragma unroll
-                for (int j = 0; j < NS; ++j) ch = fmaf(Ct[j], hcur[j], ch);
-                ch += __shfl_xor_sync(0xffffffffu, ch, 1);
-                ch += __shfl_xor_sync(0xffffffffu, ch, 2);
-                const float zt = in_z[i];
-                const float sg = rcp_approx(1.f + ex2_approx(-zt * kLog2e));
-                g = zt * sg;
-                dzt = dyt * fmaf(Dd, uu, ch) * sg * fmaf(zt, 1.f - sg, 1.f);
-            }
-            const float dyh = dyt * g;
-            float dup = 0.f, ddt = 0.f;
-#pragma unroll
-            for (int j = 0; j < NS; ++j) {
-                const float ht = hcur[j], hp = hprev[j];
-                hcur[j] = hp;
-                sdC[(i * NP + s * NS + j) * Sh::CHP + c] = dyh * ht;
-                dh[j] = fmaf(dyh, Ct[j], dh[j]);
-                const float e = ex2_approx(dl * A2[j]);
-                sdB[(i * NP + s * NS + j) * Sh::CHP + c] = dh[j] * dl * uu;
-                dup = fmaf(dh[j] * dl, Bt[j], dup);  // (Bt, Ct from the chunk's B/C rows)
-                ddt = fmaf(dh[j], fmaf(Bt[j], uu, An[j] * e * hp), ddt);
-                dAacc[j] = fmaf(dh[j] * dl, e * hp, dAacc[j]);
-                dh[j] *= e;
-            }
-            dup += __shfl_xor_sync(0xffffffffu, dup, 1);
-            dup += __shfl_xor_sync(0xffffffffu, dup, 2);
-            ddt += __shfl_xor_sync(0xffffffffu, ddt, 1);
-            ddt += __shfl_xor_sync(0xffffffffu, ddt, 2);
-            if (s == 0) {
-                const float draw = a.softplus ? ddt * rcp_approx(1.f + ex2_approx(-raw * kLog2e)) : ddt;
-                sOut[c * TC + i] = fmaf(Dd, dyh, dup);
-                sOut[(CH + c) * TC + i] = draw;
-                sOut[(2 * CH + c) * TC + i] = dzt;
-                if (valid) {
-                    dDacc = fmaf(dyh, uu, dDacc);
-                    dbacc += draw;
-                }
-            }
-        }
+        };
+        if (nt == TC)
+            sweep(std::true_type{});
+        else
+            sweep(std::false_type{});
         __syncthreads();
         // this chunk's du, ddelta, dz rows, and dB, dC summed over the CTA's channels (one atomic add
         // per CTA and element)
@@ -311,18 +333,20 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
             const int tens = q / (CH * TC), cc = (q / TC) % CH, i = q % TC;
             const long long dch = (long long)blockIdx.x * CH + cc;
             if (i < nt && dch < a.Dch)
-                IO::store(tens == 0 ? a.du : tens == 1 ? a.ddelta : a.dz, (b * a.Dch + dch) * L + t0 + i, sOut[q]);
+                IO::store(tens == 0 ? a.du : tens == 1 ? a.ddelta : a.dz, (b * a.Dch + dch) * L + t0 + i,
+                          sOut[(q / TC) * TCP + i]);
         }
         for (int q = tid; q < nt * NP; q += NTHR) {
             const int i = q / NP, n = q % NP;
             if (n < N) {
                 const float *pb = sdB + (i * NP + n) * Sh::CHP, *pc = sdC + (i * NP + n) * Sh::CHP;
-                float sb = 0.f, sc = 0.f;
-#pragma unroll 8
+                float sb4[4] = {0.f, 0.f, 0.f, 0.f}, sc4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+#pragma unroll
                 for (int cc = 0; cc < CH; ++cc) {
-                    sb += pb[cc];
-                    sc += pc[cc];
+                    sb4[cc & 3] += pb[cc];
+                    sc4[cc & 3] += pc[cc];
                 }
+                const float sb = (sb4[0] + sb4[1]) + (sb4[2] + sb4[3]), sc = (sc4[0] + sc4[1]) + (sc4[2] + sc4[3]);
                 atomicAdd(a.dB + bc0 + (long long)n * L + t0 + i, sb);
                 atomicAdd(a.dC + bc0 + (long long)n * L + t0 + i, sc);
             }
