@@ -292,20 +292,25 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
                     dzt = dyt * fmaf(Dd, uu, ch) * sg * fmaf(zt, 1.f - sg, 1.f);
                 }
                 const float dyh = dyt * g;
-                float dup = 0.f, ddt = 0.f;
+                // with dh_n after the C term and w_n = dh_n a_n h_{t-1,n}:  du gets Delta q, dDelta gets u q +
+                // sum_n A_n w_n (q = sum_n dh_n B_n), dA_n gets Delta w_n
+                const float dluu = dl * uu;
+                float q = 0.f, wa = 0.f;
 #pragma unroll
                 for (int j = 0; j < NS; ++j) {
                     const float ht = hcur[j], hp = hprev[j];
                     hcur[j] = hp;
                     sdC[(i * NP + s * NS + j) * Sh::CHP + dcol] = dyh * ht;
-                    dh[j] = fmaf(dyh, Ct[j], dh[j]);
+                    const float dhj = fmaf(dyh, Ct[j], dh[j]);
                     const float e = ex2_approx(dl * A2[j]);
-                    sdB[(i * NP + s * NS + j) * Sh::CHP + dcol] = dh[j] * dl * uu;
-                    dup = fmaf(dh[j] * dl, Bt[j], dup);  // (Bt, Ct from the chunk's B/C rows)
-                    ddt = fmaf(dh[j], fmaf(Bt[j], uu, An[j] * e * hp), ddt);
-                    dAacc[j] = fmaf(dh[j] * dl, e * hp, dAacc[j]);
-                    dh[j] *= e;
+                    sdB[(i * NP + s * NS + j) * Sh::CHP + dcol] = dhj * dluu;
+                    q = fmaf(dhj, Bt[j], q);  // (Bt, Ct from the chunk's B/C rows)
+                    const float w = dhj * (e * hp);
+                    dAacc[j] = fmaf(dl, w, dAacc[j]);
+                    wa = fmaf(An[j], w, wa);
+                    dh[j] = dhj * e;
                 }
+                float dup = dl * q, ddt = fmaf(uu, q, wa);
                 dup += __shfl_xor_sync(0xffffffffu, dup, 1);
                 dup += __shfl_xor_sync(0xffffffffu, dup, 2);
                 ddt += __shfl_xor_sync(0xffffffffu, ddt, 1);
