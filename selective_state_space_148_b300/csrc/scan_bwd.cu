@@ -100,15 +100,23 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
     const long long bc0 = b * N * L;
     const bool has_z = a.z != nullptr;
 
-    float An[NS], A2[NS], h[NS];
+    // per-state values in pairs of adjacent states (f32x2 arithmetic)
+    constexpr int NH = NS / 2;
+    float2 Anp[NH], A2p[NH], h2[NH];
     bool live[NS];
 #pragma unroll
-    for (int j = 0; j < NS; ++j) {
-        const long long n = (long long)s * NS + j;
-        live[j] = valid && n < N;
-        An[j] = live[j] ? a.A[dd * N + n] : 0.f;
-        A2[j] = An[j] * kLog2e;
-        h[j] = 0.f;
+    for (int jp = 0; jp < NH; ++jp) {
+        float v[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int j = 2 * jp + k;
+            const long long n = (long long)s * NS + j;
+            live[j] = valid && n < N;
+            v[k] = live[j] ? a.A[dd * N + n] : 0.f;
+        }
+        Anp[jp] = f2(v[0], v[1]);
+        A2p[jp] = f2(v[0] * kLog2e, v[1] * kLog2e);
+        h2[jp] = f2(0.f, 0.f);
     }
     const float Dd = (a.D != nullptr && valid) ? a.D[dd] : 0.f;
     const float bias = (a.bias != nullptr && valid) ? a.bias[dd] : 0.f;
@@ -212,21 +220,25 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
                 if (i % TC == 0) {
 #pragma unroll
                     for (int j = 0; j < NS; ++j)
-                        if (live[j]) ck[(t / TC) * N + j] = h[j];
+                        if (live[j]) ck[(t / TC) * N + j] = (j & 1) ? h2[j / 2].y : h2[j / 2].x;
                 }
                 const float dl = softplus_of(wIn[(CH + c) * TWP + i] + bias);
                 const float du = dl * wIn[c * TWP + i];
+                const float2 dl2 = f2(dl, dl), du2 = f2(du, du);
+                const float2 *wb = reinterpret_cast<const float2 *>(wB + i * NP + s * NS);
 #pragma unroll
-                for (int j = 0; j < NS; ++j)
-                    h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * wB[i * NP + s * NS + j]);
+                for (int jp = 0; jp < NH; ++jp) {
+                    const float2 x = __fmul2_rn(dl2, A2p[jp]);
+                    h2[jp] = __ffma2_rn(f2(ex2_approx(x.x), ex2_approx(x.y)), h2[jp], __fmul2_rn(du2, wb[jp]));
+                }
             }
         }
     }
 
     // ---- reverse sweep, chunk by chunk
-    float dh[NS], dAacc[NS];
+    float2 dh2[NH], dA2[NH];
 #pragma unroll
-    for (int j = 0; j < NS; ++j) dh[j] = dAacc[j] = 0.f;
+    for (int jp = 0; jp < NH; ++jp) dh2[jp] = dA2[jp] = f2(0.f, 0.f);
     float dDacc = 0.f, dbacc = 0.f;
     float hnext[NS];  // checkpoint of the next chunk to process, loaded one chunk ahead
     load_chunk((K - 1) * TC, chunk_len(K - 1), 4);
@@ -240,7 +252,9 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
         __syncthreads();
         float hstart[NS], dlr[TC];
 #pragma unroll
-        for (int j = 0; j < NS; ++j) h[j] = hstart[j] = hnext[j];
+        for (int j = 0; j < NS; ++j) hstart[j] = hnext[j];
+#pragma unroll
+        for (int jp = 0; jp < NH; ++jp) h2[jp] = f2(hnext[2 * jp], hnext[2 * jp + 1]);
         if (k > 0) {  // in flight during this chunk
             load_chunk((k - 1) * TC, TC, 4);
 #pragma unroll
@@ -256,12 +270,14 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
                     const float dl = softplus_of(in_r[i] + bias);
                     dlr[i] = dl;
                     const float du = dl * in_u[i];
-                    float Bv[NS];
-                    load_vec<NS>(Bv, sBC + i * NP + s * NS);
+                    const float2 dl2 = f2(dl, dl), du2 = f2(du, du);
+                    const float2 *bp = reinterpret_cast<const float2 *>(sBC + i * NP + s * NS);
 #pragma unroll
-                    for (int j = 0; j < NS; ++j) {
-                        h[j] = fmaf(ex2_approx(dl * A2[j]), h[j], du * Bv[j]);
-                        sH[(i * NS + j) * NTHR + tid] = h[j];
+                    for (int jp = 0; jp < NH; ++jp) {
+                        const float2 x = __fmul2_rn(dl2, A2p[jp]);
+                        h2[jp] = __ffma2_rn(f2(ex2_approx(x.x), ex2_approx(x.y)), h2[jp], __fmul2_rn(du2, bp[jp]));
+                        sH[(i * NS + 2 * jp) * NTHR + tid] = h2[jp].x;
+                        sH[(i * NS + 2 * jp + 1) * NTHR + tid] = h2[jp].y;
                     }
                 }
             }
@@ -281,9 +297,11 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
                 for (int j = 0; j < NS; ++j) hprev[j] = i > 0 ? sH[((i - 1) * NS + j) * NTHR + tid] : hstart[j];
                 float g = 1.f, dzt = 0.f;
                 if (has_z) {  // yhat = C . h_t + D u, the C . h part summed over the 4 lanes
-                    float ch = 0.f;
+                    float2 ch2 = f2(0.f, 0.f);
 #pragma unroll
-                    for (int j = 0; j < NS; ++j) ch = fmaf(Ct[j], hcur[j], ch);
+                    for (int jp = 0; jp < NH; ++jp)
+                        ch2 = __ffma2_rn(f2(Ct[2 * jp], Ct[2 * jp + 1]), f2(hcur[2 * jp], hcur[2 * jp + 1]), ch2);
+                    float ch = ch2.x + ch2.y;
                     ch += __shfl_xor_sync(0xffffffffu, ch, 1);
                     ch += __shfl_xor_sync(0xffffffffu, ch, 2);
                     const float zt = in_z[i];
@@ -295,21 +313,30 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
                 // with dh_n after the C term and w_n = dh_n a_n h_{t-1,n}:  du gets Delta q, dDelta gets u q +
                 // sum_n A_n w_n (q = sum_n dh_n B_n), dA_n gets Delta w_n
                 const float dluu = dl * uu;
-                float q = 0.f, wa = 0.f;
+                const float2 dl2 = f2(dl, dl), dluu2 = f2(dluu, dluu), dyh2 = f2(dyh, dyh);
+                float2 q2 = f2(0.f, 0.f), wa2 = f2(0.f, 0.f);
 #pragma unroll
-                for (int j = 0; j < NS; ++j) {
-                    const float ht = hcur[j], hp = hprev[j];
-                    hcur[j] = hp;
-                    sdC[(i * NP + s * NS + j) * Sh::CHP + dcol] = dyh * ht;
-                    const float dhj = fmaf(dyh, Ct[j], dh[j]);
-                    const float e = ex2_approx(dl * A2[j]);
-                    sdB[(i * NP + s * NS + j) * Sh::CHP + dcol] = dhj * dluu;
-                    q = fmaf(dhj, Bt[j], q);  // (Bt, Ct from the chunk's B/C rows)
-                    const float w = dhj * (e * hp);
-                    dAacc[j] = fmaf(dl, w, dAacc[j]);
-                    wa = fmaf(An[j], w, wa);
-                    dh[j] = dhj * e;
+                for (int jp = 0; jp < NH; ++jp) {
+                    const int j = 2 * jp;
+                    const float2 ht = f2(hcur[j], hcur[j + 1]), hp = f2(hprev[j], hprev[j + 1]);
+                    hcur[j] = hp.x;
+                    hcur[j + 1] = hp.y;
+                    const float2 tc = __fmul2_rn(dyh2, ht);
+                    sdC[(i * NP + s * NS + j) * Sh::CHP + dcol] = tc.x;
+                    sdC[(i * NP + s * NS + j + 1) * Sh::CHP + dcol] = tc.y;
+                    const float2 dhj = __ffma2_rn(dyh2, f2(Ct[j], Ct[j + 1]), dh2[jp]);
+                    const float2 x = __fmul2_rn(dl2, A2p[jp]);
+                    const float2 e = f2(ex2_approx(x.x), ex2_approx(x.y));
+                    const float2 tb = __fmul2_rn(dhj, dluu2);
+                    sdB[(i * NP + s * NS + j) * Sh::CHP + dcol] = tb.x;
+                    sdB[(i * NP + s * NS + j + 1) * Sh::CHP + dcol] = tb.y;
+                    q2 = __ffma2_rn(dhj, f2(Bt[j], Bt[j + 1]), q2);  // (Bt, Ct from the chunk's B/C rows)
+                    const float2 w = __fmul2_rn(dhj, __fmul2_rn(e, hp));
+                    dA2[jp] = __ffma2_rn(dl2, w, dA2[jp]);
+                    wa2 = __ffma2_rn(Anp[jp], w, wa2);
+                    dh2[jp] = __fmul2_rn(dhj, e);
                 }
+                const float q = q2.x + q2.y, wa = wa2.x + wa2.y;
                 float dup = dl * q, ddt = fmaf(uu, q, wa);
                 dup += __shfl_xor_sync(0xffffffffu, dup, 1);
                 dup += __shfl_xor_sync(0xffffffffu, dup, 2);
@@ -359,7 +386,7 @@ scan_bwd_kernel(const BwdArgs a, long long K) {
     }
 #pragma unroll
     for (int j = 0; j < NS; ++j)
-        if (live[j]) atomicAdd(a.dA + dd * N + (long long)s * NS + j, dAacc[j]);
+        if (live[j]) atomicAdd(a.dA + dd * N + (long long)s * NS + j, (j & 1) ? dA2[j / 2].y : dA2[j / 2].x);
     if (valid && s == 0) {
         if (a.dD != nullptr) atomicAdd(a.dD + dd, dDacc);
         if (a.dbias != nullptr) atomicAdd(a.dbias + dd, dbacc);
