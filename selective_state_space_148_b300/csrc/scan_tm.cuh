@@ -16,7 +16,10 @@
 //   D[m][col] = sum_k Sel[m][k] * X[col][k],   Sel[m][k] = 1 iff k selects slice (m mod 4)
 //
 // X holds, per pair of steps (t, t+1), 16 columns j: B_{4s+j/2} at step t+j%2
-// for j < 8, C_{4s+(j-8)/2} at step t+j%2 for j >= 8, with the four slices'
+// for j < 8, C_{4s+(j-8)/2} at step t+j%2 for j >= 8 (the end-state pass of
+// the chunked scan, which reads no C, orders each 8-step sub-tile's 64 columns
+// as its 32 B columns then its 32 C columns and loads only the first half),
+// with the four slices'
 // values along K (bf16 storage: one bf16 each, exact; fp32 storage: each value
 // split into three bf16 parts hi+mid+lo whose fp32 sum reproduces it, K rows
 // 3s..3s+2).  D lands in TMEM as fp32; thread m reads its lane with
@@ -252,16 +255,26 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         tc::tma_load_3d(st + Sh::OFF_BC + Sh::BC_TILE, &maps.C, x, 0, (int)b, bar);
     };
 
-    // X of one super-tile from its stage: column n = 16 * pair + j (column order
-    // above), K row k = slice k's value (bf16), or K rows 3k..3k+2 its three
-    // bf16 parts (fp32, S = 4)
+    // X of one super-tile from its stage: column n = 16 * pair + j (MODE_FULL) or
+    // 64 * sub-tile + 32 * (B or C) + 8 * pair-in-sub-tile + j (MODE_STATES), the
+    // column orders above; K row k = slice k's value (bf16), or K rows 3k..3k+2
+    // its three bf16 parts (fp32, S = 4)
     auto x_build = [&](int xb, const unsigned char *st) {  // by the producer warp
         const T *raw = reinterpret_cast<const T *>(st + Sh::OFF_BC);  // [which][4 S][TT]
         unsigned char *xbase = sX + xb * Sh::X_BYTES;
         for (int n = lane; n < COLS; n += 32) {
-            const int j = n & 15;
-            const int t = 2 * (n >> 4) + (j & 1);
-            const int which = j >> 3, col = (j & 7) >> 1;
+            int t, which, col;
+            if constexpr (MODE == MODE_FULL) {
+                const int j = n & 15;
+                t = 2 * (n >> 4) + (j & 1);
+                which = j >> 3;
+                col = (j & 7) >> 1;
+            } else {
+                const int j = n & 7;
+                t = 8 * (n >> 6) + 2 * ((n >> 3) & 3) + (j & 1);
+                which = (n >> 5) & 1;
+                col = j >> 1;
+            }
             float v[S];
 #pragma unroll
             for (int sl = 0; sl < S; ++sl) {
@@ -442,10 +455,16 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
             const int r0 = sup * TT + 2 * ps;  // this lane's pair offset in sub-tile 0 of this super-tile
 #pragma unroll
             for (int q = 0; q < NSUB; ++q) {
+                // MODE_FULL: step pairs 0, 1 in bcu[0] and 2, 3 in bcu[1], 16 columns each;
+                // MODE_STATES: B of the 4 step pairs in bcu[0] (8 columns each), no C
                 uint32_t bcu[2][32];
                 tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64, bcu[0]);
-                tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64 + 32, bcu[1]);
-                tc::tmem_wait_ld_tied(bcu[0], bcu[1]);
+                if constexpr (MODE == MODE_FULL) {
+                    tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64 + 32, bcu[1]);
+                    tc::tmem_wait_ld_tied(bcu[0], bcu[1]);
+                } else {
+                    tc::tmem_wait_ld_tied(bcu[0]);
+                }
 
                 // one block: y of sub-tile i-1, Delta etc. of sub-tile i+1, the
                 // recurrence of sub-tile i (i = 4 sup + q, so i & 1 == q & 1)
@@ -465,7 +484,8 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                 for (int p = 0; p < TB / 2; ++p) {
                     const float2 dl = f2(dq[p].x, dq[p].y);
                     const float2 du = f2(dq[p].z, dq[p].w);
-                    const uint32_t *bcp = bcu[p >> 1] + 16 * (p & 1);
+                    const uint32_t *bcp = MODE == MODE_FULL ? bcu[p >> 1] + 16 * (p & 1) : bcu[0] + 8 * p;
+                    const uint32_t *ccp = bcp + 8;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const float2 x = __fmul2_rn(dl, A2d[j]);
@@ -474,10 +494,10 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                         hh[j].y = fmaf(ex2_approx(x.y), hh[j].x, bu.y);
                     }
                     if (MODE == MODE_FULL) {
-                        float2 P = __fmul2_rn(f2(__uint_as_float(bcp[8]), __uint_as_float(bcp[9])), hh[0]);
-                        P = __ffma2_rn(f2(__uint_as_float(bcp[10]), __uint_as_float(bcp[11])), hh[1], P);
-                        P = __ffma2_rn(f2(__uint_as_float(bcp[12]), __uint_as_float(bcp[13])), hh[2], P);
-                        P = __ffma2_rn(f2(__uint_as_float(bcp[14]), __uint_as_float(bcp[15])), hh[3], P);
+                        float2 P = __fmul2_rn(f2(__uint_as_float(ccp[0]), __uint_as_float(ccp[1])), hh[0]);
+                        P = __ffma2_rn(f2(__uint_as_float(ccp[2]), __uint_as_float(ccp[3])), hh[1], P);
+                        P = __ffma2_rn(f2(__uint_as_float(ccp[4]), __uint_as_float(ccp[5])), hh[2], P);
+                        P = __ffma2_rn(f2(__uint_as_float(ccp[6]), __uint_as_float(ccp[7])), hh[3], P);
                         pq[2 * p] = P.x;
                         pq[2 * p + 1] = P.y;
                     }
