@@ -214,6 +214,17 @@ def time_oracle(x, budget_s=12.0):
     return bytes_s, nch * N * L / t, dict(channels=nch, of=chans_total, seconds=t, threads=threads)
 
 
+def time_oracle_threads(x, threads, budget_s=8.0):
+    """time_oracle with the oracle limited to `threads` host threads."""
+    import oracle
+    n0 = oracle.num_threads()
+    oracle.set_num_threads(threads)
+    try:
+        return time_oracle(x, budget_s=budget_s)
+    finally:
+        oracle.set_num_threads(n0)
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -226,6 +237,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time only the headline workload (by default a run of the default workload at N=1 also "
+                         "times every other workload into the line's 'workloads' object)")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass of the scan (gradients of sum(dy * y)) on the workload")
     ap.add_argument("--conv", default="none", choices=["none", "fused", "two-step"],
@@ -261,6 +275,12 @@ def main():
     else:
         res = bench_scan(args, m, torch)
 
+    extra = None
+    if world == 1 and not decode and not args.backward and args.conv == "none" and \
+            args.workload == DEFAULT_WORKLOAD and not args.no_workloads:
+        torch.cuda.empty_cache()
+        extra = other_workloads(args, m, torch)
+
     # max over ranks of the timed regions; every rank ran the same per-rank workload (weak scaling)
     t_ms, res["e2e_ms"] = max_over_ranks([res["ms_per_step"], res["e2e_ms"]], dist, torch, "cuda")
     value, e2e_value = aggregate_gbs(world, res["bytes"], t_ms, res["e2e_ms"])
@@ -274,6 +294,11 @@ def main():
                "sample": f"float64 oracle over whole time rows of {info['channels']} of {info['of']} channels "
                          f"of {args.workload} ({info['seconds']:.1f} s); value scaled to the workload's bytes",
                "updates_per_s": ups}
+        bps1, ups1, info1 = time_oracle_threads(res["inputs"], 1, budget_s=8.0)
+        cpu["single_thread"] = {
+            "value": bps1 / 1e9, "unit": "GB/s", "cores": 1, "updates_per_s": ups1,
+            "sample": f"the same oracle on one thread: whole time rows of {info1['channels']} channels "
+                      f"({info1['seconds']:.1f} s)"}
 
     if rank == 0:
         line = {
@@ -295,10 +320,55 @@ def main():
             "clocks": res["clocks"],
             "mufu": res.get("mufu"),
         }
+        if res.get("chained") is not None:
+            line["chained"] = res["chained"]
+        if extra is not None:
+            line["workloads"] = extra
         print(json.dumps(line))
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+# the other workloads timed into the default run's 'workloads' object: name -> timed steps
+OTHER_SCAN_WORKLOADS = {"mamba2p8b_b4_d5120_n16_l4096_bf16": 40, "mamba2p8b_b4_d5120_n64_l4096_bf16": 12,
+                        "dna_b1_d1536_n16_l1048576_bf16": 5}
+
+
+def workload_entry(res):
+    """The per-workload summary kept in the 'workloads' object."""
+    t = res["ms_per_step"]
+    e = {"ms_per_step": round(t, 6), "value": round(res["bytes"] / (t * 1e-3) / 1e9, 2), "unit": "GB/s",
+         "tokens_per_s": round(res["tokens"] / (t * 1e-3), 1), "steps": res.get("steps"),
+         "roofline": res["roofline"], "clocks": res["clocks"], "config": res["config"],
+         "gpu_launches": res["launches"]}
+    if res.get("chained") is not None:
+        e["chained"] = res["chained"]
+    return e
+
+
+def other_workloads(args, m, torch):
+    """Every other workload of the benchmark, each timed in this run with its own clock record."""
+    out = {}
+    for name, k in OTHER_SCAN_WORKLOADS.items():
+        r = bench_scan(args, m, torch, workload=name, steps=k, e2e=False, conv="none")
+        r["steps"] = k
+        out[name] = workload_entry(r)
+        del r
+        torch.cuda.empty_cache()
+    r = bench_decode(args, m, torch, steps=inputs.DECODE_WORKLOAD["steps"], e2e=False)
+    r["steps"] = inputs.DECODE_WORKLOAD["steps"]
+    out[inputs.DECODE_WORKLOAD["name"]] = workload_entry(r)
+    torch.cuda.empty_cache()
+    r = bench_scan(args, m, torch, workload=DEFAULT_WORKLOAD, steps=100, e2e=False, conv="fused")
+    r["steps"] = 100
+    out[DEFAULT_WORKLOAD + "+conv_fused"] = workload_entry(r)
+    torch.cuda.empty_cache()
+    r = bench_backward(args, m, torch, workload=DEFAULT_WORKLOAD, steps=20, e2e=False)
+    r["steps"] = 20
+    out[DEFAULT_WORKLOAD + "+backward"] = workload_entry(r)
+    torch.cuda.empty_cache()
+    return out
 
 
 def pipelined_e2e(torch, steps, upload, compute, download, nbuf=2):
@@ -379,8 +449,11 @@ def kernel_source_sha(sources=SCAN_KERNEL_SOURCES):
     return h.hexdigest()[:16]
 
 
-def bench_scan(args, m, torch):
-    x = inputs.make_workload(args.workload)
+def bench_scan(args, m, torch, workload=None, steps=None, e2e=True, conv=None):
+    workload = workload or args.workload
+    steps = steps or args.steps
+    conv = args.conv if conv is None else conv
+    x = inputs.make_workload(workload)
     Bsz, Dch, L, N = x.shape
     io = x.io
     tdt = torch.bfloat16 if io == "bf16" else torch.float32
@@ -403,17 +476,17 @@ def bench_scan(args, m, torch):
     ws_bytes = m.mamba_scan_workspace_size(Bsz, Dch, L, N, 0, m.MAMBA_BF16 if io == "bf16" else m.MAMBA_F32)
     chunked = ws_bytes > 0
     stream = torch.cuda.current_stream()
-    if args.conv != "none":   # s["u"] then holds x, the convolution's input
+    if conv != "none":   # s["u"] then holds x, the convolution's input
         cw, cb = (torch.from_numpy(a).to(dev) for a in inputs.conv_params(Dch, 7))
         u_tmp = torch.empty_like(base["u"])
 
     def run(s, y, h, st=None, ut=None):
         st = stream if st is None else st
-        ut = u_tmp if ut is None and args.conv == "two-step" else ut
-        if args.conv == "fused":
+        ut = u_tmp if ut is None and conv == "two-step" else ut
+        if conv == "fused":
             m.mamba_selective_scan_fwd_conv(s["u"], cw, cb, s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h,
                                             stream=st)
-        elif args.conv == "two-step":
+        elif conv == "two-step":
             m.mamba_causal_conv1d_silu(s["u"], cw, cb, 1, ut, stream=st)
             m.mamba_selective_scan_fwd(ut, s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h, stream=st)
         else:
@@ -430,20 +503,28 @@ def bench_scan(args, m, torch):
     with ClockSampler(pci_bus_id(torch)) as cs:
         torch.cuda.synchronize()
         ev0.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             step(i)
         ev1.record(stream)
         torch.cuda.synchronize()
-    t_ms = ev0.elapsed_time(ev1) / args.steps
+    t_ms = ev0.elapsed_time(ev1) / steps
     clocks = cs.summary()
 
     # end to end through the C ABI from pinned host buffers (uploads and downloads overlap the neighbouring
     # steps' kernels; two device buffer sets)
+    e2e_ms, h2d, d2h = None, None, None
+    if e2e:
+        e2e_ms, h2d, d2h = scan_e2e(args, torch, base, sets, ys, hs, run, conv, tdt, Bsz, Dch, N)
+    return scan_result(args, m, torch, x, workload, steps, conv, t_ms, clocks, chunked, nbytes, R, e2e_ms, h2d, d2h,
+                       mufu_per_clk, sms)
+
+
+def scan_e2e(args, torch, base, sets, ys, hs, run, conv, tdt, Bsz, Dch, N):
     hsrc = {k: v.cpu().pin_memory() for k, v in base.items()}
     hy = [torch.empty(base["u"].shape, dtype=tdt).pin_memory() for _ in range(2)]
     hh = [torch.empty((Bsz, Dch, N), dtype=torch.float32).pin_memory() for _ in range(2)]
     dsets = [sets[0], sets[1]]
-    utmp = [torch.empty_like(base["u"]) for _ in range(2)] if args.conv == "two-step" else [None, None]
+    utmp = [torch.empty_like(base["u"]) for _ in range(2)] if conv == "two-step" else [None, None]
 
     def upload(k, st):
         for n in dsets[k]:
@@ -460,7 +541,13 @@ def bench_scan(args, m, torch):
     e2e_ms = pipelined_e2e(torch, args.e2e_steps, upload, compute, download)
     h2d = sum(v.numel() * v.element_size() for v in hsrc.values())
     d2h = hy[0].numel() * hy[0].element_size() + hh[0].numel() * hh[0].element_size()
+    return e2e_ms, h2d, d2h
 
+
+def scan_result(args, m, torch, x, workload, steps, conv, t_ms, clocks, chunked, nbytes, R, e2e_ms, h2d, d2h,
+                mufu_per_clk, sms):
+    Bsz, Dch, L, N = x.shape
+    io = x.io
     peaks = measured_peaks()
     exps = Bsz * Dch * L * N
     t_hbm = nbytes / (peaks["hbm_gbs"] * 1e9)
@@ -470,9 +557,9 @@ def bench_scan(args, m, torch):
     t_meas = t_ms * 1e-3
     tm = 8 < N <= 64 and (io == "bf16" or N <= 16) and os.environ.get("MAMBA_SCAN_KERNEL") != "smem"
     kernel = (f"scan_tm_kernel<{io},full,z,S{4 if N <= 16 else 8 if N <= 32 else 16}"
-              f"{',conv' if args.conv == 'fused' else ''}>" if tm
+              f"{',conv' if conv == 'fused' else ''}>" if tm
               else f"scan_kernel<{io},NP{1 << max(2, (N - 1).bit_length())},full>")
-    traffic = traffic_record(f"{args.workload}")
+    traffic = traffic_record(workload)
     if t_mufu >= t_hbm:
         roof = {"bound": "alu", "achieved": round(exps / t_meas / 1e12, 4),
                 "peak": round(mufu_peak / 1e12, 4), "unit": "Tex2/s", "frac": round(t_mufu / t_meas, 4),
@@ -487,23 +574,24 @@ def bench_scan(args, m, torch):
                 "peak_source": f"{peaks['source']} copy bandwidth"}
     if chunked:
         roof["note"] = "chunked scan: the step is three launches (chunk states, carry, rescan); figures are per step"
-    if args.conv == "two-step":
+    if conv == "two-step":
         roof["note"] = (roof.get("note", "") + "; " if "note" in roof else "") + \
             "two launches per step (convolution, then scan); figures are per step"
     return dict(ms_per_step=t_ms, bytes=nbytes, tokens=Bsz * L, dtype="f32" if io == "f32" else "bf16",
-                config={"workload": args.workload, "batch": Bsz, "d_inner": Dch, "d_state": N, "seq_len": L,
+                config={"workload": workload, "batch": Bsz, "d_inner": Dch, "d_state": N, "seq_len": L,
                         "io": io, "state": "fp32", "l2": f"inputs rotate over {R} resident copies "
                                                           f"({R * nbytes / 1e6:.0f} MB > L2)",
                         "path": "chunked" if chunked else "direct",
-                        **({"conv": args.conv + " (depthwise causal conv1d k=4 + SiLU feeding u)"}
-                           if args.conv != "none" else {})},
+                        **({"conv": conv + " (depthwise causal conv1d k=4 + SiLU feeding u)"}
+                           if conv != "none" else {})},
                 roofline=roof, h2d=h2d, d2h=d2h, e2e_ms=e2e_ms,
-                launches=args.steps * ((3 if chunked else 1) + (1 if args.conv == "two-step" else 0)),
+                launches=steps * ((3 if chunked else 1) + (1 if conv == "two-step" else 0)),
                 clocks=clocks, inputs=x,
                 mufu={"ex2_per_clk_per_sm": round(mufu_per_clk, 3), "sms": sms})
 
 
-def bench_decode(args, m, torch):
+def bench_decode(args, m, torch, steps=None, e2e=True):
+    steps = steps or args.steps
     cfg = inputs.DECODE_WORKLOAD
     Bsz, Dch, N, io = cfg["batch"], cfg["dim"], cfg["dstate"], cfg["io"]
     dev = torch.device("cuda")
@@ -542,7 +630,7 @@ def bench_decode(args, m, torch):
     cap.wait_stream(stream)
     with torch.cuda.stream(cap):
         with torch.cuda.graph(graph, stream=cap):
-            for i in range(args.steps):
+            for i in range(steps):
                 m.mamba_state_update(states[i % R], steps_in[i % P]["u"], steps_in[i % P]["delta"], A,
                                      steps_in[i % P]["B"], steps_in[i % P]["C"], D, steps_in[i % P]["z"], bias, 1,
                                      ys[i % R], stream=cap)
@@ -555,7 +643,28 @@ def bench_decode(args, m, torch):
         graph.replay()
         ev1.record(stream)
         torch.cuda.synchronize()
-    t_ms = ev0.elapsed_time(ev1) / args.steps
+    t_ms = ev0.elapsed_time(ev1) / steps
+    clocks = cs.summary()
+
+    # the same steps launched one by one from the host (no graph): what a caller that does not capture pays
+    ch_steps = min(steps, 200)
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    with ClockSampler(pci_bus_id(torch)) as cs2:
+        ev0.record(stream)
+        for i in range(ch_steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    chained_ms = ev0.elapsed_time(ev1) / ch_steps
+    chained = {"ms_per_step": round(chained_ms, 6), "steps": ch_steps,
+               "value": round(nbytes / (chained_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "frac": round(nbytes / (measured_peaks()["hbm_gbs"] * 1e9) / (chained_ms * 1e-3), 4),
+               "clocks": cs2.summary(), "launch": "one host launch per step, chained on one stream"}
+    if not e2e:
+        return decode_result(args, m, torch, steps, t_ms, clocks, nbytes, R, None, None, None, mufu_per_clk, sms,
+                             chained)
 
     # end to end: every step uploads the state and the step's inputs from pinned host memory and downloads
     # y and the new state; uploads and downloads overlap the neighbouring steps' kernels (two buffer sets)
@@ -581,6 +690,13 @@ def bench_decode(args, m, torch):
     e2e_ms = pipelined_e2e(torch, args.e2e_steps, upload, compute, download)
     h2d = hst[0].numel() * 4 + sum(v.numel() * v.element_size() for v in hin[0].values())
     d2h = hy[0].numel() * 2 + hst[0].numel() * 4
+    return decode_result(args, m, torch, steps, t_ms, clocks, nbytes, R, e2e_ms, h2d, d2h, mufu_per_clk, sms,
+                         chained)
+
+
+def decode_result(args, m, torch, steps, t_ms, clocks, nbytes, R, e2e_ms, h2d, d2h, mufu_per_clk, sms, chained):
+    cfg = inputs.DECODE_WORKLOAD
+    Bsz, Dch, N, io = cfg["batch"], cfg["dim"], cfg["dstate"], cfg["io"]
     peaks = measured_peaks()
     t_meas = t_ms * 1e-3
     roof = {"bound": "hbm", "achieved": round(nbytes / t_meas / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
@@ -591,9 +707,9 @@ def bench_decode(args, m, torch):
                 config={"workload": cfg["name"], "batch": Bsz, "d_inner": Dch, "d_state": N, "io": io,
                         "state": "fp32", "l2": f"state rotates over {R} resident copies "
                                                 f"({R * nbytes / 1e6:.0f} MB > L2)",
-                        "launch": f"the {args.steps} timed steps replayed as one captured CUDA graph"},
-                roofline=roof, h2d=h2d, d2h=d2h, e2e_ms=e2e_ms, launches=args.steps, clocks=cs.summary(),
-                mufu={"ex2_per_clk_per_sm": round(mufu_per_clk, 3), "sms": sms})
+                        "launch": f"the {steps} timed steps replayed as one captured CUDA graph"},
+                roofline=roof, h2d=h2d, d2h=d2h, e2e_ms=e2e_ms, launches=steps, clocks=clocks,
+                mufu={"ex2_per_clk_per_sm": round(mufu_per_clk, 3), "sms": sms}, chained=chained)
 
 
 def bwd_bytes(Bsz, Dch, L, N, io):
@@ -603,8 +719,10 @@ def bwd_bytes(Bsz, Dch, L, N, io):
     return 7 * Bsz * Dch * L * s + 2 * Bsz * N * L * s + 2 * Bsz * N * L * 4 + 2 * Dch * N * 4 + 6 * Dch * 4
 
 
-def bench_backward(args, m, torch):
-    x = inputs.make_workload(args.workload)
+def bench_backward(args, m, torch, workload=None, steps=None, e2e=True):
+    workload = workload or args.workload
+    steps = steps or args.steps
+    x = inputs.make_workload(workload)
     Bsz, Dch, L, N = x.shape
     io = x.io
     dev = torch.device("cuda")
@@ -632,18 +750,47 @@ def bench_backward(args, m, torch):
         m.mamba_selective_scan_bwd(s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, s["dy"], o["du"],
                                    o["dd"], o["dA"], o["dB"], o["dC"], o["dD"], o["dz"], o["db"], stream=stream)
 
+    mufu_per_clk, sms = mufu_ex2_per_clk_per_sm(m, torch)
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(pci_bus_id(torch)) as cs:
         ev0.record(stream)
-        for i in range(args.steps):
+        for i in range(steps):
             step(i)
         ev1.record(stream)
         torch.cuda.synchronize()
-    t_ms = ev0.elapsed_time(ev1) / args.steps
+    t_ms = ev0.elapsed_time(ev1) / steps
 
+    clocks = cs.summary()
+    e2e_ms, h2d, d2h = None, None, None
+    if e2e:
+        e2e_ms, h2d, d2h = bwd_e2e(args, torch, t, sets, outs, step, stream)
+    peaks = measured_peaks()
+    t_meas = t_ms * 1e-3
+    exps = Bsz * Dch * L * N
+    mufu_units = round(mufu_per_clk)
+    mufu_peak = SM_COUNT_NOMINAL * mufu_units * peaks["sm_max_mhz"] * 1e6
+    roof = {"bound": "alu", "achieved": round(exps / t_meas / 1e12, 4), "peak": round(mufu_peak / 1e12, 4),
+            "unit": "Tex2/s", "frac": round(exps / mufu_peak / t_meas, 4), "traffic": None,
+            "kernel": f"scan_bwd_kernel<{io},NS{4 if N <= 16 else 8 if N <= 32 else 16}>",
+            "peak_source": f"{SM_COUNT_NOMINAL} SMs x {mufu_units} ex2/clk/SM (microbenchmark: "
+                           f"{mufu_per_clk:.2f}) x {peaks['sm_max_mhz']:.0f} MHz",
+            "note": "algorithmic exps count B·D·L·N once; the kernel evaluates them three times (checkpoint "
+                    "sweep, chunk recompute, reverse sweep)",
+            "hbm": {"achieved": round(nbytes / t_meas / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": round(nbytes / (peaks["hbm_gbs"] * 1e9) / t_meas, 4)}}
+    return dict(ms_per_step=t_ms, bytes=nbytes, tokens=Bsz * L, dtype="f32" if io == "f32" else "bf16",
+                config={"workload": workload, "pass": "backward", "batch": Bsz, "d_inner": Dch, "d_state": N,
+                        "seq_len": L, "io": io, "grads": "du, ddelta, dz (storage type); dA, dB, dC, dD, dbias fp32",
+                        "l2": f"inputs rotate over {R} resident copies"},
+                roofline=roof, h2d=h2d, d2h=d2h, e2e_ms=e2e_ms,
+                launches=steps,  # the backward kernel (plus five cudaMemsetAsync zero fills per step)
+                clocks=clocks, inputs=x, mufu={"ex2_per_clk_per_sm": round(mufu_per_clk, 3), "sms": sms})
+
+
+def bwd_e2e(args, torch, t, sets, outs, step, stream):
     # end to end: inputs from pinned host memory, every gradient back to the host
     hin = {k: v.cpu().pin_memory() for k, v in t.items()}
     hout = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs[0].items()}
@@ -665,25 +812,8 @@ def bench_backward(args, m, torch):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
-    peaks = measured_peaks()
-    t_meas = t_ms * 1e-3
-    exps = Bsz * Dch * L * N
-    mufu_peak = SM_COUNT_NOMINAL * 32 * peaks["sm_max_mhz"] * 1e6
-    roof = {"bound": "alu", "achieved": round(exps / t_meas / 1e12, 4), "peak": round(mufu_peak / 1e12, 4),
-            "unit": "Tex2/s", "frac": round(exps / mufu_peak / t_meas, 4), "traffic": None,
-            "kernel": f"scan_bwd_kernel<{io},NS{4 if N <= 16 else 8 if N <= 32 else 16}>",
-            "note": "algorithmic exps count B·D·L·N once; the kernel evaluates them three times (checkpoint "
-                    "sweep, chunk recompute, reverse sweep)",
-            "hbm": {"achieved": round(nbytes / t_meas / 1e9, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                    "frac": round(nbytes / (peaks["hbm_gbs"] * 1e9) / t_meas, 4)}}
-    return dict(ms_per_step=t_ms, bytes=nbytes, tokens=Bsz * L, dtype="f32" if io == "f32" else "bf16",
-                config={"workload": args.workload, "pass": "backward", "batch": Bsz, "d_inner": Dch, "d_state": N,
-                        "seq_len": L, "io": io, "grads": "du, ddelta, dz (storage type); dA, dB, dC, dD, dbias fp32",
-                        "l2": f"inputs rotate over {R} resident copies"},
-                roofline=roof, h2d=sum(v.numel() * v.element_size() for v in hin.values()),
-                d2h=sum(v.numel() * v.element_size() for v in hout.values()), e2e_ms=e2e_ms,
-                launches=args.steps,  # the backward kernel (plus five cudaMemsetAsync zero fills per step)
-                clocks=cs.summary(), inputs=x)
+    return e2e_ms, sum(v.numel() * v.element_size() for v in hin.values()), \
+        sum(v.numel() * v.element_size() for v in hout.values())
 
 
 def reference_arm(args, world, rank):

@@ -69,7 +69,7 @@ enum mamba_status {
     MAMBA_ERR_BAD_DTYPE = -4,       /* dtype is not MAMBA_F32 / MAMBA_BF16 */
     MAMBA_ERR_ALLOC = -5,           /* stream-ordered workspace allocation failed */
     MAMBA_ERR_LAUNCH = -6,          /* a kernel launch failed (cudaGetLastError) */
-    MAMBA_ERR_DEVICE_TIMEOUT = -7,  /* reserved: a bounded device-side wait expired */
+    MAMBA_ERR_DEVICE_TIMEOUT = -7,  /* a bounded device-side wait expired (mamba_device_error) */
     MAMBA_ERR_BAD_FLAGS = -8,       /* unknown bit in `flags` */
     MAMBA_ERR_WORKSPACE = -9,       /* caller workspace too small or misaligned */
     MAMBA_ERR_DEVICE = -10,         /* no usable CUDA device / query failed */
@@ -226,10 +226,12 @@ int mamba_selective_scan_fwd_conv(const void *x, const float *conv_w, const floa
  * every GPU that loads the library holds until the process exits.
  *
  * Arguments are those of mamba_selective_scan_fwd_ex without flags and
- * workspace; chunk_len must be >= 1 (rounded up to the kernel's time tile).
- * When one chunk covers the sequence the direct scan runs and no scratch is
- * touched.  Needs Bsz*K*Dch*(N+1)*4 bytes (each part rounded up to 256), K =
- * ceil(L / chunk_len); larger problems return MAMBA_ERR_SCRATCH_LIMIT before
+ * workspace; chunk_len must be >= 1.  The chunks are c = chunk_len rounded up
+ * to the kernel's time tile (16 steps for N <= 8, 32 steps otherwise) long, so
+ * there are K = ceil(L / c) of them.  When one chunk covers the sequence the
+ * direct scan runs and no scratch is touched.  Otherwise the call needs
+ * Bsz*K*Dch*N*4 + Bsz*K*Dch*4 bytes of scratch (each part rounded up to a
+ * multiple of 256); larger problems return MAMBA_ERR_SCRATCH_LIMIT before
  * anything is launched.  No cudaMalloc/cudaFree or allocating library call
  * is made.
  *
@@ -253,6 +255,15 @@ int mamba_selective_scan_fwd_noalloc(const void *u, const void *delta, const flo
  * (synchronous).  Returns MAMBA_ERR_DEVICE_TIMEOUT if a bounded device-side
  * wait of an earlier kernel gave up (that kernel's outputs are then invalid),
  * MAMBA_OK otherwise, MAMBA_ERR_DEVICE if the query fails.
+ *
+ * The waits in question are those of the tensor-memory scan kernel (input
+ * tiles landed, selector MMA done, buffer released by every compute warp),
+ * each limited to 2^24 polls.  Test hook: with the environment variable
+ * MAMBA_TEST_WAIT_POLLS=n (read on the host at every call, n < 2^24) the
+ * limit is n polls, so a small n makes the kernel give up and take its abort
+ * path -- it still waits, with the full limit, for its own copies and MMAs in
+ * flight before it frees tensor memory and returns -- and this function then
+ * reports MAMBA_ERR_DEVICE_TIMEOUT.
  */
 int mamba_device_error(void);
 

@@ -131,6 +131,27 @@ def state_update(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, soft
     return y, st
 
 
+def state_update_inplace(state, u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus_flag=True,
+                         disc=DISC_SIMPLE):
+    """The step of ``state_update`` applied to ``state`` itself (a C-contiguous float64 array, overwritten
+    with the new state); returns y[b,d].  For long chains over large states, where copying the state at
+    every step would dominate."""
+    if not (isinstance(state, np.ndarray) and state.dtype == np.float64 and state.flags.c_contiguous):
+        raise TypeError("state must be a C-contiguous float64 array")
+    u, delta, A, B, C = (_f64(x) for x in (u, delta, A, B, C))
+    D, z, delta_bias = (_f64(x) for x in (D, z, delta_bias))
+    Bsz, Dch, N = state.shape
+    if N > 4096:
+        raise ValueError("oracle supports N <= 4096")
+    assert u.shape == (Bsz, Dch) and delta.shape == (Bsz, Dch)
+    assert B.shape == (Bsz, N) and C.shape == (Bsz, N) and A.shape == (Dch, N)
+    y = np.empty((Bsz, Dch), dtype=np.float64)
+    _load().oracle_state_update(_ptr(state), _ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                _ptr(z), _ptr(delta_bias), int(bool(softplus_flag)), int(disc), _ptr(y),
+                                Bsz, Dch, N)
+    return y
+
+
 def causal_conv1d(x, w, bias=None, silu=True):
     """Depthwise causal convolution (width W = w.shape[1]) of x [Bsz, Dch, L], then SiLU.
 

@@ -27,6 +27,7 @@ STATUS = {
     -4: "MAMBA_ERR_BAD_DTYPE", -5: "MAMBA_ERR_ALLOC", -6: "MAMBA_ERR_LAUNCH", -7: "MAMBA_ERR_DEVICE_TIMEOUT",
     -8: "MAMBA_ERR_BAD_FLAGS", -9: "MAMBA_ERR_WORKSPACE", -10: "MAMBA_ERR_DEVICE", -11: "MAMBA_ERR_SCRATCH_LIMIT",
 }
+STATUS_CODE = {name: code for code, name in STATUS.items()}
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 _lib = None

@@ -1,6 +1,8 @@
 // scan_tm.cu -- instantiations and launch of the tensor-memory scan kernel
 // (TMA descriptors, launch geometry), and the device error word it reports
 // bounded-wait timeouts in.
+#include <cstdlib>
+
 #include <cuda.h>
 
 #include "../../include/mamba_scan.h"
@@ -121,7 +123,21 @@ cudaError_t launch_tm_s(int mode, const ScanArgs &a, const TmMaps &maps, int war
 
 }  // namespace
 
-cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &a, long long Bsz, int grid_chunks, cudaStream_t st) {
+// Poll limit of the kernel's pipeline waits: 2^24 polls (a few tens of nanoseconds each, so well
+// under a second), or the value of MAMBA_TEST_WAIT_POLLS, a host-side test hook that makes the waits give
+// up early so that the abort path and the device error word can be exercised without any fault.
+static unsigned pipeline_wait_polls() {
+    const char *v = std::getenv("MAMBA_TEST_WAIT_POLLS");
+    if (v == nullptr || *v == '\0') return 1u << 24;
+    char *end = nullptr;
+    const unsigned long n = std::strtoul(v, &end, 10);
+    return (end != nullptr && *end == '\0' && n < (1ul << 24)) ? (unsigned)n : (1u << 24);
+}
+
+cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &args, long long Bsz, int grid_chunks,
+                           cudaStream_t st) {
+    ScanArgs a = args;
+    a.wait_polls = pipeline_wait_polls();
     // TMA coordinates are 32-bit: the time axis and the channel axis must fit
     if (a.L >= (1LL << 31) - 64 || a.Dch >= (1LL << 31) - 128 || Bsz >= (1LL << 31)) return cudaErrorNotSupported;
     const bool bf16 = dtype == 1;

@@ -134,7 +134,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     constexpr bool FAST = sizeof(T) == 2;
     constexpr int S = Sh::S, TT = Sh::TT, TB = Sh::TB, NSUB = Sh::NSUB, COLS = Sh::COLS, MAX_CH = Sh::MAX_CH;
     constexpr int NST = Sh::NST;
-    constexpr uint32_t kWaitPolls = 1u << 24;
+    constexpr uint32_t kWaitPolls = 1u << 24;  // drain waits before TMEM and shared memory are released
     constexpr uint32_t kIdesc = tc::umma_idesc_bf16_f32(128, COLS);
     using Word = typename std::conditional<Sh::SPLIT, float2, uint32_t>::type;  // one step pair
 
@@ -229,7 +229,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     // bounded wait that gives up at once when another warp has already given up;
     // the producer backs off between polls (its waits last up to a super-tile)
     auto wait_or_abort = [&](uint64_t *bar, uint32_t parity, bool backoff) -> bool {
-        const uint32_t polls = backoff ? kWaitPolls / 8 : kWaitPolls;
+        const uint32_t polls = backoff ? a.wait_polls / 8 : a.wait_polls;
         for (uint32_t it = 0;; ++it) {
             if (tc::mbar_test_wait(bar, parity)) return true;
             if (*abort_flag != 0 || it >= polls) return false;
@@ -343,7 +343,9 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         const float2 m0 = unpack(*reinterpret_cast<const Word *>(xr));      // x_t, x_{t+1}
         const float p0 = fmaf(cw.w, m0.x, fmaf(cw.z, m2.y, fmaf(cw.y, m2.x, fmaf(cw.x, m4.y, cb))));
         const float p1 = fmaf(cw.w, m0.y, fmaf(cw.z, m0.x, fmaf(cw.y, m2.y, fmaf(cw.x, m2.x, cb))));
-        return silu2<FAST>(f2(p0, p1));
+        // u feeds the fp32 state, so it takes the accurate SiLU (z / (1 + e^-z), ~1e-6 relative), not
+        // the one-MUFU tanh form whose ~2^-11 error would carry into last_state
+        return silu2<false>(f2(p0, p1));
     };
     float4 *const du_chan = sDU + c * 4;  // + (i & 1) * MAX_CH * 4 + pair
     // Delta, Delta * u of this lane's pair at offset r (sub-tile parity par) ->

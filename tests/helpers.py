@@ -54,19 +54,3 @@ def dev_inputs(x: "inputs.ScanInputs"):
     """All scan inputs of a ScanInputs on the GPU."""
     return dict(u=to_dev(x.u, x.io), delta=to_dev(x.delta, x.io), z=to_dev(x.z, x.io), B=to_dev(x.B, x.io),
                 C=to_dev(x.C, x.io), A=f32_dev(x.A), D=f32_dev(x.D), delta_bias=f32_dev(x.delta_bias))
-
-
-def oracle_rows(x: "inputs.ScanInputs", chans, softplus=True, h0=None, disc=0, reverse=False, with_z=True):
-    """Oracle y and last_state for a list of (b, d) channels only."""
-    import oracle
-    ys, hs = [], []
-    for (b, d) in chans:
-        sl = lambda a: None if a is None else inputs.to_f64(a[b:b + 1, d:d + 1], x.io)
-        y, h = oracle.selective_scan(sl(x.u), sl(x.delta), x.A[d:d + 1].astype(np.float64),
-                                     inputs.to_f64(x.B[b:b + 1], x.io), inputs.to_f64(x.C[b:b + 1], x.io),
-                                     x.D[d:d + 1].astype(np.float64), sl(x.z) if with_z else None,
-                                     x.delta_bias[d:d + 1].astype(np.float64), softplus_flag=softplus,
-                                     h0=None if h0 is None else h0[b:b + 1, d:d + 1], disc=disc, reverse=reverse)
-        ys.append(y[0, 0])
-        hs.append(h[0, 0])
-    return np.stack(ys), np.stack(hs)

@@ -65,15 +65,6 @@ def test_decode_optional_inputs():
     chain(2, 33, 16, 10, "bf16", seed=33, with_z=False, with_D=False)
 
 
-def test_decode_full_workload_1000_steps():
-    cfg = inputs.DECODE_WORKLOAD
-    rng = np.random.default_rng(5)
-    sample = sorted({(int(rng.integers(cfg["batch"])), int(rng.integers(cfg["dim"]))) for _ in range(48)}
-                    | {(0, 0), (cfg["batch"] - 1, cfg["dim"] - 1)})
-    ey, es = chain(cfg["batch"], cfg["dim"], cfg["dstate"], cfg["steps"], cfg["io"], cfg["seed"], sample=sample)
-    print(f"decode full 1000 steps: y {ey:.3g} state {es:.3g}")
-
-
 def test_scan_then_step_equals_longer_scan():
     """scan over t < L, then one decode step for token L, matches the oracle scan over L + 1 tokens."""
     import torch

@@ -1,8 +1,8 @@
 """Parity of the CUDA selective scan (through the C ABI) with the float64 oracle.
 
-Small and mid sizes are compared element by element on every output; the full
-workload sizes are compared on sampled channels (whole time rows and final
-states), which the oracle computes one by one.
+Small and mid sizes, element by element on every output (the full-size
+workloads are in test_full_size_gpu.py).  Every call is followed by a check
+that no bounded device-side wait of the kernels gave up.
 """
 import numpy as np
 import pytest
@@ -10,7 +10,7 @@ import pytest
 import oracle
 import selective_state_space_148_b300 as m
 from selective_state_space_148_b300 import inputs
-from helpers import (TOL_STATE, TOL_Y, assert_close, dev_inputs, f32_dev, oracle_rows, to_dev, to_host_f64)
+from helpers import TOL_STATE, TOL_Y, assert_close, dev_inputs, f32_dev, to_host_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -31,6 +31,7 @@ def run_gpu(x, softplus=True, with_z=True, with_D=True, with_bias=True, h0=None,
                                       t["z"] if with_z else None, t["delta_bias"] if with_bias else None, softplus,
                                       y, last, h0=h0d, flags=flags, chunk_len=chunk_len)
     torch.cuda.synchronize()
+    assert m.mamba_device_error() == 0
     return to_host_f64(y), (last.cpu().numpy().astype(np.float64) if want_last else None)
 
 
@@ -214,38 +215,6 @@ def test_caller_workspace_and_errors(monkeypatch):
     assert_close(to_host_f64(y), yr, TOL_Y["bf16"], "direct y under injected allocation failure")
 
 
-# ----------------------------------------------------------------------------- full-size workloads, sampled
-
-def sample_channels(Bsz, Dch, k=10, seed=123):
-    rng = np.random.default_rng(seed)
-    ch = {(0, 0), (Bsz - 1, Dch - 1), (Bsz - 1, 0), (0, Dch - 1)}
-    while len(ch) < k:
-        ch.add((int(rng.integers(Bsz)), int(rng.integers(Dch))))
-    return sorted(ch)
-
-
-@pytest.mark.parametrize("name", ["mamba130m_b8_d1536_n16_l2048_bf16", "mamba2p8b_b4_d5120_n16_l4096_bf16",
-                                  "mamba2p8b_b4_d5120_n64_l4096_bf16", "dna_b1_d1536_n16_l1048576_bf16"])
-def test_full_workload_sampled(name):
-    import torch
-    x = inputs.make_workload(name)
-    Bsz, Dch, L, N = x.shape
-    t = dev_inputs(x)
-    y = torch.empty_like(t["u"])
-    h = torch.empty((Bsz, Dch, N), dtype=torch.float32, device="cuda")
-    m.mamba_selective_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], 1, y, h)
-    torch.cuda.synchronize()
-    chans = sample_channels(Bsz, Dch, k=6 if L > 100000 else 12)
-    yr, hr = oracle_rows(x, chans)
-    yg = np.stack([to_host_f64(y[b, d]) for (b, d) in chans])
-    hg = np.stack([h[b, d].cpu().numpy() for (b, d) in chans]).astype(np.float64)
-    ey = assert_close(yg, yr, TOL_Y["bf16"], f"{name} y")
-    eh = assert_close(hg, hr, TOL_STATE, f"{name} state")
-    # properties that hold everywhere: finite outputs
-    assert torch.isfinite(y.float()).all() and torch.isfinite(h).all()
-    print(f"{name}: y err ratio {ey:.3g}, state {eh:.3g}, chunked={m.mamba_scan_workspace_size(Bsz, Dch, L, N) > 0}")
-
-
 # ----------------------------------------------------------------------------- flags: exact ZOH, reverse scan
 
 FLAG_CASES = {  # name -> (flags, oracle disc, oracle reverse)
@@ -326,3 +295,28 @@ def test_aligned_state_sizes(N, L):
     yr, hr = run_oracle(x, h0=h0.astype(np.float64))
     assert_close(yg, yr, TOL_Y["bf16"], f"aligned chunked N={N} L={L} y")
     assert_close(hg, hr, TOL_STATE, f"aligned chunked N={N} L={L} last_state")
+
+
+# ----------------------------------------------------------------------------- bounded waits: the abort path
+
+def test_bounded_wait_gives_up_and_reports_timeout(monkeypatch):
+    """With its pipeline waits capped at zero polls (the MAMBA_TEST_WAIT_POLLS hook), the tensor-memory
+    kernel gives up at its first wait for an input tile, takes the abort path (it still drains its own
+    copies and MMAs before freeing tensor memory) and the device error word reports the timeout; the
+    next call without the hook runs normally and matches the oracle."""
+    import torch
+    x = inputs.make_scan_inputs(2, 45, 16, 256, io="bf16", seed=95)   # aligned bf16, N = 16: tensor-memory kernel
+    assert m.mamba_device_error() == 0
+    monkeypatch.setenv("MAMBA_TEST_WAIT_POLLS", "0")
+    t = dev_inputs(x)
+    y = torch.empty_like(t["u"])
+    last = torch.empty((2, 45, 16), dtype=torch.float32, device="cuda")
+    for chunk_len in (-1, 64):                 # the direct scan, then both kernels of the chunked scan
+        m.mamba_selective_scan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"],
+                                      1, y, last, chunk_len=chunk_len)
+        torch.cuda.synchronize()
+        assert m.mamba_device_error() == m.STATUS_CODE["MAMBA_ERR_DEVICE_TIMEOUT"]
+        assert m.mamba_device_error() == 0     # read and cleared
+    monkeypatch.delenv("MAMBA_TEST_WAIT_POLLS")
+    ey, eh = check(x, "after an aborted call")
+    print(f"after the aborted calls: y err ratio {ey:.3g}, state {eh:.3g}")

@@ -47,6 +47,8 @@ def test_noalloc_matches_chunked_entry_point_on_two_calls(io):
                                       y_ref, h_ref, h0=h0, chunk_len=chunk_len)
         y = torch.full_like(t["u"], float("nan"))
         h = torch.full((2, 40, 16), float("nan"), dtype=torch.float32, device="cuda")
+        torch.cuda.synchronize()
+        before = (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0])
         st = m.lib().mamba_selective_scan_fwd_noalloc(
             t["u"].data_ptr(), t["delta"].data_ptr(), t["A"].data_ptr(), t["B"].data_ptr(), t["C"].data_ptr(),
             t["D"].data_ptr(), t["z"].data_ptr(), t["delta_bias"].data_ptr(), 1, y.data_ptr(), h.data_ptr(),
@@ -54,5 +56,9 @@ def test_noalloc_matches_chunked_entry_point_on_two_calls(io):
             chunk_len, torch.cuda.current_stream().cuda_stream)
         assert st == 0, m.status_string(st)
         torch.cuda.synchronize()
+        if call:
+            # after the first call (which looks up the array's address and may load the kernels), a call
+            # changes neither torch's allocation count nor the device's free memory
+            assert (torch.cuda.memory_allocated(), torch.cuda.mem_get_info()[0]) == before
         assert_close(to_host_f64(y), to_host_f64(y_ref), TOL_Y[io], f"call {call} y")
         assert_close(h.cpu().numpy(), h_ref.cpu().numpy(), TOL_STATE, f"call {call} last_state")
