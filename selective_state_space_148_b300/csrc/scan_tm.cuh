@@ -54,7 +54,7 @@
 // predicated store by lanes s < 4) and runs the recurrence over sub-tile i's
 // 8 steps.
 //
-// Every mbarrier wait is bounded; a timeout sets a shared abort flag that
+// Every mbarrier wait is bounded (about a second); a timeout sets a shared abort flag that
 // every later wait honours and that stops further loads and MMAs, is recorded
 // in the device error word, and the CTA still walks its loop (its results are
 // then meaningless), waits (bounded) for its issued MMAs and loads, frees its
@@ -226,14 +226,17 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     // y of the step at offset r from t_begin in this lane's channel: ylane + r
     T *const ylane = reinterpret_cast<T *>(a.y) + ((b * a.Dch + dd) * L + t_begin);
 
-    // bounded wait that gives up at once when another warp has already given up;
-    // the producer backs off between polls (its waits last up to a super-tile)
-    auto wait_or_abort = [&](uint64_t *bar, uint32_t parity, bool backoff) -> bool {
-        const uint32_t polls = backoff ? a.wait_polls / 8 : a.wait_polls;
-        for (uint32_t it = 0;; ++it) {
-            if (tc::mbar_test_wait(bar, parity)) return true;
-            if (*abort_flag != 0 || it >= polls) return false;
-            if (backoff) __nanosleep(32);
+    // Bounded wait that gives up at once when another warp has already given up: a non-blocking test,
+    // then try_wait calls that suspend the thread in hardware until the phase completes (at most 20 us
+    // each; a waiting warp spends no issue slots) until one second of the global timer has passed.  With
+    // a.wait_polls == 0 (test hook) the wait gives up after the first test.
+    auto wait_or_abort = [&](uint64_t *bar, uint32_t parity, bool) -> bool {
+        if (tc::mbar_test_wait(bar, parity)) return true;
+        if (a.wait_polls == 0 || *abort_flag != 0) return false;
+        const uint64_t t0 = tc::globaltimer_ns();
+        for (;;) {
+            if (tc::mbar_try_wait(bar, parity, 20000u)) return true;
+            if (*abort_flag != 0 || tc::globaltimer_ns() - t0 > 1000000000ull) return false;
         }
     };
 

@@ -49,6 +49,23 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *mbar, uint32_t parity) 
         : "memory");
     return ok != 0;
 }
+// potentially blocking probe: the thread may be suspended in hardware until the
+// phase completes or about suspend_ns nanoseconds pass (no issue slots spent)
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *mbar, uint32_t parity, uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(mbar)), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+// nanoseconds of the global timer
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
 // Bounded wait: returns false if the phase did not complete within max_iter
 // non-blocking polls (a few tens of nanoseconds each, so the bound is well under
 // a second).
