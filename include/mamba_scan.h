@@ -258,12 +258,12 @@ int mamba_selective_scan_fwd_noalloc(const void *u, const void *delta, const flo
  *
  * The waits in question are those of the tensor-memory scan kernel (input
  * tiles landed, selector MMA done, buffer released by every compute warp),
- * each limited to 2^24 polls.  Test hook: with the environment variable
- * MAMBA_TEST_WAIT_POLLS=n (read on the host at every call, n < 2^24) the
- * limit is n polls, so a small n makes the kernel give up and take its abort
- * path -- it still waits, with the full limit, for its own copies and MMAs in
- * flight before it frees tensor memory and returns -- and this function then
- * reports MAMBA_ERR_DEVICE_TIMEOUT.
+ * each limited to about one second of the GPU's global timer.  Test hook:
+ * with the environment variable MAMBA_TEST_WAIT_POLLS=0 (read on the host at
+ * every call) every such wait gives up after one non-blocking test, so the
+ * kernel takes its abort path -- it still waits, with a fixed limit, for its
+ * own copies and MMAs in flight before it frees tensor memory and returns --
+ * and this function then reports MAMBA_ERR_DEVICE_TIMEOUT.
  */
 int mamba_device_error(void);
 

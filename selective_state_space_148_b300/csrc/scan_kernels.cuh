@@ -49,8 +49,9 @@ struct ScanArgs {
     long long chunk_len;  // steps per chunk (multiple of TT); L for the direct scan
     int nchunks;          // K
     int softplus;
-    // tensor-memory kernel: polls after which a pipeline wait (loads landed, MMA done, buffer free) gives
-    // up and the kernel takes its abort path; the drain waits before TMEM is freed keep their own limit
+    // tensor-memory kernel: 0 makes a pipeline wait (loads landed, MMA done, buffer free) give up after
+    // one test (test hook), anything else bounds it at about a second; the drain waits before TMEM is
+    // freed keep their own limit
     unsigned wait_polls;
     int flags;            // MAMBA_FLAG_ZOH (1) | MAMBA_FLAG_REVERSE (2); honoured by the GEN instantiation only
     // non-null: `u` holds x and u = SiLU(causal width-4 conv of x) is formed in

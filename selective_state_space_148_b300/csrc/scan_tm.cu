@@ -123,9 +123,9 @@ cudaError_t launch_tm_s(int mode, const ScanArgs &a, const TmMaps &maps, int war
 
 }  // namespace
 
-// Poll limit of the kernel's pipeline waits: 2^24 polls (a few tens of nanoseconds each, so well
-// under a second), or the value of MAMBA_TEST_WAIT_POLLS, a host-side test hook that makes the waits give
-// up early so that the abort path and the device error word can be exercised without any fault.
+// The kernel's pipeline waits are bounded by time (about a second); MAMBA_TEST_WAIT_POLLS=0, a host-side
+// test hook, makes them give up after one test so that the abort path and the device error word can be
+// exercised without any fault.  Any other value keeps the normal bound.
 static unsigned pipeline_wait_polls() {
     const char *v = std::getenv("MAMBA_TEST_WAIT_POLLS");
     if (v == nullptr || *v == '\0') return 1u << 24;
