@@ -242,6 +242,8 @@ def main():
                          "times every other workload into the line's 'workloads' object)")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass of the scan (gradients of sum(dy * y)) on the workload")
+    ap.add_argument("--flags", default="none", choices=["none", "zoh", "reverse", "zoh+reverse"],
+                    help="scan flags: the exact zero-order hold and/or the reverse-time scan")
     ap.add_argument("--conv", default="none", choices=["none", "fused", "two-step"],
                     help="feed the scan through the depthwise causal conv1d + SiLU branch: fused into the scan "
                          "kernel, or as a separate convolution launch before the scan")
@@ -351,7 +353,7 @@ def other_workloads(args, m, torch):
     """Every other workload of the benchmark, each timed in this run with its own clock record."""
     out = {}
     for name, k in OTHER_SCAN_WORKLOADS.items():
-        r = bench_scan(args, m, torch, workload=name, steps=k, e2e=False, conv="none")
+        r = bench_scan(args, m, torch, workload=name, steps=k, e2e=False, conv="none", flag_name="none")
         r["steps"] = k
         out[name] = workload_entry(r)
         del r
@@ -364,6 +366,11 @@ def other_workloads(args, m, torch):
     r["steps"] = 100
     out[DEFAULT_WORKLOAD + "+conv_fused"] = workload_entry(r)
     torch.cuda.empty_cache()
+    for fl in ("zoh", "reverse"):
+        r = bench_scan(args, m, torch, workload=DEFAULT_WORKLOAD, steps=100, e2e=False, conv="none", flag_name=fl)
+        r["steps"] = 100
+        out[DEFAULT_WORKLOAD + "+" + fl] = workload_entry(r)
+        torch.cuda.empty_cache()
     r = bench_backward(args, m, torch, workload=DEFAULT_WORKLOAD, steps=20, e2e=False)
     r["steps"] = 20
     out[DEFAULT_WORKLOAD + "+backward"] = workload_entry(r)
@@ -449,10 +456,15 @@ def kernel_source_sha(sources=SCAN_KERNEL_SOURCES):
     return h.hexdigest()[:16]
 
 
-def bench_scan(args, m, torch, workload=None, steps=None, e2e=True, conv=None):
+FLAG_BITS = {"none": 0, "zoh": 1, "reverse": 2, "zoh+reverse": 3}
+
+
+def bench_scan(args, m, torch, workload=None, steps=None, e2e=True, conv=None, flag_name=None):
     workload = workload or args.workload
     steps = steps or args.steps
     conv = args.conv if conv is None else conv
+    flag_name = (args.flags if flag_name is None else flag_name) if conv == "none" else "none"
+    flags = FLAG_BITS[flag_name]
     x = inputs.make_workload(workload)
     Bsz, Dch, L, N = x.shape
     io = x.io
@@ -489,6 +501,9 @@ def bench_scan(args, m, torch, workload=None, steps=None, e2e=True, conv=None):
         elif conv == "two-step":
             m.mamba_causal_conv1d_silu(s["u"], cw, cb, 1, ut, stream=st)
             m.mamba_selective_scan_fwd(ut, s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h, stream=st)
+        elif flags:
+            m.mamba_selective_scan_fwd_ex(s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h,
+                                          flags=flags, stream=st)
         else:
             m.mamba_selective_scan_fwd(s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, y, h, stream=st)
 
@@ -516,7 +531,7 @@ def bench_scan(args, m, torch, workload=None, steps=None, e2e=True, conv=None):
     if e2e:
         e2e_ms, h2d, d2h = scan_e2e(args, torch, base, sets, ys, hs, run, conv, tdt, Bsz, Dch, N)
     return scan_result(args, m, torch, x, workload, steps, conv, t_ms, clocks, chunked, nbytes, R, e2e_ms, h2d, d2h,
-                       mufu_per_clk, sms)
+                       mufu_per_clk, sms, flag_name)
 
 
 def scan_e2e(args, torch, base, sets, ys, hs, run, conv, tdt, Bsz, Dch, N):
@@ -545,7 +560,7 @@ def scan_e2e(args, torch, base, sets, ys, hs, run, conv, tdt, Bsz, Dch, N):
 
 
 def scan_result(args, m, torch, x, workload, steps, conv, t_ms, clocks, chunked, nbytes, R, e2e_ms, h2d, d2h,
-                mufu_per_clk, sms):
+                mufu_per_clk, sms, flag_name="none"):
     Bsz, Dch, L, N = x.shape
     io = x.io
     peaks = measured_peaks()
@@ -557,7 +572,7 @@ def scan_result(args, m, torch, x, workload, steps, conv, t_ms, clocks, chunked,
     t_meas = t_ms * 1e-3
     tm = 8 < N <= 64 and (io == "bf16" or N <= 16) and os.environ.get("MAMBA_SCAN_KERNEL") != "smem"
     kernel = (f"scan_tm_kernel<{io},full,z,S{4 if N <= 16 else 8 if N <= 32 else 16}"
-              f"{',conv' if conv == 'fused' else ''}>" if tm
+              f"{',conv' if conv == 'fused' else ''}{',flags' if flag_name != 'none' else ''}>" if tm
               else f"scan_kernel<{io},NP{1 << max(2, (N - 1).bit_length())},full>")
     traffic = traffic_record(workload)
     if t_mufu >= t_hbm:
@@ -582,6 +597,7 @@ def scan_result(args, m, torch, x, workload, steps, conv, t_ms, clocks, chunked,
                         "io": io, "state": "fp32", "l2": f"inputs rotate over {R} resident copies "
                                                           f"({R * nbytes / 1e6:.0f} MB > L2)",
                         "path": "chunked" if chunked else "direct",
+                        **({"flags": flag_name} if flag_name != "none" else {}),
                         **({"conv": conv + " (depthwise causal conv1d k=4 + SiLU feeding u)"}
                            if conv != "none" else {})},
                 roofline=roof, h2d=h2d, d2h=d2h, e2e_ms=e2e_ms,

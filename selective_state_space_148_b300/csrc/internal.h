@@ -47,6 +47,12 @@ cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &a, long long Bsz
 cudaError_t launch_carry(const float *A, const float *h0, float *ws_h, const float *ws_sdt, long long Bsz,
                          long long Dch, long long N, int K, cudaStream_t st);
 
+// Read and clear the device error words of the tensor-memory scan's translation units (its plain, reverse
+// and zero-order-hold instantiations); MAMBA_OK or MAMBA_ERR_DEVICE.
+int tm_read_clear_error(unsigned int *v);
+int tm_rev_read_clear_error(unsigned int *v);
+int tm_zoh_read_clear_error(unsigned int *v);
+
 struct StepArgs {
     float *state;
     const void *u, *delta, *z, *Bm, *Cm;

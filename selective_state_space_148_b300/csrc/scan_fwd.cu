@@ -76,7 +76,7 @@ static cudaError_t launch_t(int mode, bool vec, const ScanArgs &a, long long Bsz
 }
 
 // The tensor-memory kernel serves 8 < N <= 64 (bf16; fp32 up to N = 16) on the
-// 16-byte aligned path without flags; MAMBA_SCAN_KERNEL=smem selects the
+// 16-byte aligned path, with or without flags; MAMBA_SCAN_KERNEL=smem selects the
 // shared-memory kernel instead (for comparison, or where tensor memory cannot
 // be used).
 static bool use_tmem_kernel() {
@@ -101,9 +101,9 @@ cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long l
     // Its TMA boxes start on 32-step boundaries, so chunks must be whole
     // super-tiles; it declines (cudaErrorNotSupported) what its descriptors
     // cannot express and fp32 with N > 16.  N <= 8 keeps the shared-memory
-    // kernel (one or two lanes per channel).
-    if (vec && a.flags == 0 && a.N > 8 && a.N <= 64 && (a.nchunks == 1 || a.chunk_len % 32 == 0) &&
-        use_tmem_kernel()) {
+    // kernel (one or two lanes per channel), and so do flagged calls on
+    // unaligned data (its general instantiation).
+    if (vec && a.N > 8 && a.N <= 64 && (a.nchunks == 1 || a.chunk_len % 32 == 0) && use_tmem_kernel()) {
         const cudaError_t e = launch_scan_tm(dtype, mode, a, Bsz, grid_chunks, st);
         if (e != cudaErrorNotSupported) return e;
     }

@@ -1,6 +1,8 @@
 // scan_tm.cu -- instantiations and launch of the tensor-memory scan kernel
-// (TMA descriptors, launch geometry), and the device error word it reports
-// bounded-wait timeouts in.
+// (TMA descriptors, launch geometry), and the device error word its
+// instantiations here report bounded-wait timeouts in (the instantiations that
+// honour the scan flags live in scan_tm_rev.cu and scan_tm_zoh.cu, with words of
+// their own).
 #include <cstdlib>
 
 #include <cuda.h>
@@ -9,7 +11,7 @@
 #include "internal.h"
 
 namespace mamba {
-__device__ unsigned int g_device_error = 0;
+static __device__ unsigned int g_device_error = 0;
 }  // namespace mamba
 
 #include "scan_tm.cuh"
@@ -93,34 +95,6 @@ int choose_warps(long long Bsz, long long Dch, int grid_chunks, int sms, int S) 
     return w;
 }
 
-template <typename T, int MODE, bool HAS_Z, int S, bool CONV = false>
-cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int grid_chunks,
-                          cudaStream_t st) {
-    using Sh = TmShape<T, MODE, S, CONV>;
-    auto kern = scan_tm_kernel<T, MODE, HAS_Z, S, CONV>;
-    static bool attr_set[kMaxDevices] = {};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < kMaxDevices) attr_set[dev] = true;
-    }
-    const long long ch = 32LL * warps / S;
-    dim3 grid((unsigned)((a.Dch + ch - 1) / ch), (unsigned)Bsz, (unsigned)grid_chunks);
-    kern<<<grid, 32 * (warps + 1), Sh::SMEM_BYTES, st>>>(a, maps);  // + the producer warp
-    return cudaGetLastError();
-}
-
-template <typename T, int S>
-cudaError_t launch_tm_s(int mode, const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int gc,
-                        cudaStream_t st) {
-    if (mode == MODE_STATES) return launch_tm_one<T, MODE_STATES, false, S>(a, maps, warps, Bsz, gc, st);
-    return a.z != nullptr ? launch_tm_one<T, MODE_FULL, true, S>(a, maps, warps, Bsz, gc, st)
-                          : launch_tm_one<T, MODE_FULL, false, S>(a, maps, warps, Bsz, gc, st);
-}
-
 }  // namespace
 
 // The kernel's pipeline waits are bounded by time (about a second); MAMBA_TEST_WAIT_POLLS=0, a host-side
@@ -158,6 +132,8 @@ cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &args, long long 
                     encode_3d(&maps.B, a.Bm, bf16, a.L, a.N, Bsz, 4u * S, false) &&
                     encode_3d(&maps.C, a.Cm, bf16, a.L, a.N, Bsz, 4u * S, false);
     if (!ok) return cudaErrorNotSupported;
+    if (a.flags & SCAN_FLAG_ZOH) return launch_tm_zoh(dtype, S, mode, a, maps, warps, Bsz, grid_chunks, st);
+    if (a.flags & SCAN_FLAG_REVERSE) return launch_tm_rev(dtype, S, mode, a, maps, warps, Bsz, grid_chunks, st);
     if (conv)
         return mode == MODE_STATES
                    ? launch_tm_one<bf16_t, MODE_STATES, false, 4, true>(a, maps, warps, Bsz, grid_chunks, st)
@@ -172,15 +148,14 @@ cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &args, long long 
 
 }  // namespace mamba
 
+namespace mamba {
+int tm_read_clear_error(unsigned int *v) { return read_clear_word(g_device_error, v); }
+}  // namespace mamba
+
 extern "C" int mamba_device_error(void) {
-    unsigned int v = 0, zero = 0;
-    if (cudaMemcpyFromSymbol(&v, mamba::g_device_error, sizeof(v)) != cudaSuccess) {
-        cudaGetLastError();
+    unsigned int v = 0, r = 0, z = 0;
+    if (mamba::tm_read_clear_error(&v) != MAMBA_OK || mamba::tm_rev_read_clear_error(&r) != MAMBA_OK ||
+        mamba::tm_zoh_read_clear_error(&z) != MAMBA_OK)
         return MAMBA_ERR_DEVICE;
-    }
-    if (v != 0 && cudaMemcpyToSymbol(mamba::g_device_error, &zero, sizeof(zero)) != cudaSuccess) {
-        cudaGetLastError();
-        return MAMBA_ERR_DEVICE;
-    }
-    return v != 0 ? MAMBA_ERR_DEVICE_TIMEOUT : MAMBA_OK;
+    return (v | r | z) != 0 ? MAMBA_ERR_DEVICE_TIMEOUT : MAMBA_OK;
 }

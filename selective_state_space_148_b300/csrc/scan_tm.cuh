@@ -68,9 +68,10 @@
 
 namespace mamba {
 
-// Device error word (defined by the one translation unit that includes this
-// header, scan_tm.cu, before the include).  Bit 0: an mbarrier wait of the
-// tensor-memory scan timed out.
+// Device error word: each translation unit that includes this header defines
+// its own g_device_error (static, before the include) and reports it through
+// mamba_device_error.  Bit 0: an mbarrier wait of the tensor-memory scan
+// timed out.
 
 // TMA descriptors of one call: u, Delta_raw, z as [Bsz][Dch][L] with boxes of
 // 32 steps x 8W channels (swizzled); B, C as [Bsz][N][L] with boxes of 32
@@ -78,6 +79,8 @@ namespace mamba {
 struct TmMaps {
     CUtensorMap u, delta, z, B, C;
 };
+
+enum { FL_REV = 1, FL_ZOH = 2 };  // flag variants of the kernel (template argument FLAGS)
 
 // S = lanes per channel (4, 8 or 16: N <= 4 S), each lane owning 4 states.
 // CONV: the first input tile is x with an 8-step halo (40 steps from t0 - 8,
@@ -126,8 +129,12 @@ struct TmShape {
 // HAS_Z: the gate z is given (MODE_FULL only).  S lanes per channel.  CONV:
 // a.u holds x and u = SiLU(a.conv_b + causal width-4 conv with a.conv_w) is
 // formed here (ai.xwebgame.com summary, "running it in PyTorch" block).
+// FLAGS (compile time): 0 the plain scan; FL_REV the scan over t = L-1 .. 0
+// (SCAN_FLAG_REVERSE; fsdata.site explainer §7 table, the reverse SSM);
+// FL_ZOH the exact zero-order-hold input weight (freeguideonline tutorial
+// §2.2), forwards or, with SCAN_FLAG_REVERSE, in reverse.
 // blockDim.x = 32 (W + 1): W compute warps (8..11) and one producer warp.
-template <typename T, int MODE, bool HAS_Z, int S_, bool CONV = false>
+template <typename T, int MODE, bool HAS_Z, int S_, bool CONV = false, int FLAGS = 0>
 __global__ void __launch_bounds__(TmShape<T, MODE, S_, CONV>::LAUNCH_THR, 1)
 scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     using Sh = TmShape<T, MODE, S_, CONV>;
@@ -201,6 +208,8 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     // per-lane constants and state (states n = 4s + j).  A2d[j] = (A_n log2 e, A_n log2 e);
     // hh[j] = (h_n(t), h_n(t+1)) of the last step pair, .y the current state.
     float2 A2d[4], hh[4];
+    constexpr bool zoh = FLAGS == FL_ZOH;
+    float invA[zoh ? 4 : 1], aZero[zoh ? 4 : 1];  // ZOH: 1/A_n (0 where A_n = 0) and [A_n = 0]
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const long long n = 4LL * s + j;
@@ -209,7 +218,13 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         if (a.hin != nullptr && valid && n < N) hn = a.hin[((b * a.nchunks + kch) * a.Dch + dd) * N + n];
         A2d[j] = f2(an, an);
         hh[j] = f2(0.f, hn);
+        if constexpr (zoh) {
+            invA[j] = an != 0.f ? kLog2e / an : 0.f;
+            aZero[j] = an == 0.f ? 1.f : 0.f;
+        }
     }
+    // FL_REV is launched only for reverse scans; FL_ZOH serves both directions
+    const bool rev = FLAGS == FL_REV || (FLAGS == FL_ZOH && (a.flags & SCAN_FLAG_REVERSE) != 0);
     const float Dd = (a.D != nullptr && valid) ? a.D[dd] : 0.f;
     const float bias = (a.bias != nullptr && valid) ? a.bias[dd] : 0.f;
     const float2 bias2 = f2(bias, bias);
@@ -223,8 +238,10 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
             cb = a.conv_b != nullptr ? a.conv_b[dd] : 0.f;
         }
     }
-    // y of the step at offset r from t_begin in this lane's channel: ylane + r
-    T *const ylane = reinterpret_cast<T *>(a.y) + ((b * a.Dch + dd) * L + t_begin);
+    // y of the (logical) step at offset r from t_begin in this lane's channel: ylane[r] forwards, the
+    // physical row mirrored in reverse (logical step tau sits at L - 1 - tau)
+    T *const yrow = reinterpret_cast<T *>(a.y) + (b * a.Dch + dd) * L;
+    T *const ylane = yrow + t_begin;
 
     // Bounded wait that gives up at once when another warp has already given up: a non-blocking test,
     // then try_wait calls that suspend the thread in hardware until the phase completes (at most 20 us
@@ -247,7 +264,10 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     auto load_stage = [&](int sn) {
         unsigned char *st = stage_of(sn % NST);
         uint64_t *bar = &io[sn % NST];
-        const int x = (int)(t_begin + (long long)sn * TT);
+        // forwards: the box of logical steps tau0 .. tau0 + 31 starts at tau0; reverse: it covers physical
+        // steps L - 32 - tau0 .. L - 1 - tau0 (a negative start of the last one reads zeros)
+        const long long tau0 = t_begin + (long long)sn * TT;
+        const int x = (int)(rev ? L - TT - tau0 : tau0);
         const uint32_t first = CONV ? (uint32_t)(ch * Sh::XSTEPS * (int)sizeof(T)) : (uint32_t)(ch * Sh::ROW);
         tc::mbar_arrive_expect_tx(bar, first + (uint32_t)((HAS_Z ? 2 : 1) * ch * Sh::ROW + 2 * Sh::BC_TILE));
         // CONV: x from 8 steps back (a negative start reads zeros: the causal padding)
@@ -278,6 +298,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                 which = (n >> 5) & 1;
                 col = j >> 1;
             }
+            if (rev) t = TT - 1 - t;  // logical step t of the super-tile sits at box position 31 - t
             float v[S];
 #pragma unroll
             for (int sl = 0; sl < S; ++sl) {
@@ -329,9 +350,12 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     int sw_off[NSUB];  // swizzled byte offset of this lane's pair in sub-tile q
 #pragma unroll
     for (int q = 0; q < NSUB; ++q) {
-        const int o = c * Sh::ROW + (q * TB + 2 * ps) * (int)sizeof(T);
+        // reverse: logical steps i, i + 1 sit at box positions 31 - i, 30 - i, i.e. in the word at 30 - i
+        const int pos = rev ? TT - 2 - (q * TB + 2 * ps) : q * TB + 2 * ps;
+        const int o = c * Sh::ROW + pos * (int)sizeof(T);
         sw_off[q] = o ^ (((o >> 7) & (Sh::SWZ - 1)) << 4);
     }
+    auto order = [&](float2 v) { return rev ? f2(v.y, v.x) : v; };  // box pair -> (step i, step i + 1)
     // tensor 0 = u (or x), 1 = Delta_raw, 2 = z
     auto stage_word = [&](const unsigned char *st, int tensor, int q) -> Word {
         return *reinterpret_cast<const Word *>(st + (tensor == 0 ? 0 : Sh::X0_TILE + (tensor - 1) * Sh::IO_TILE) +
@@ -358,16 +382,17 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         const bool in = (unsigned)r < lenv;
         float2 u;
         if constexpr (CONV) u = conv_u(st, q);
-        else u = unpack(stage_word(st, 0, q));
-        const float2 raw = __fadd2_rn(unpack(stage_word(st, 1, q)), bias2);
+        else u = order(unpack(stage_word(st, 0, q)));
+        const float2 raw = __fadd2_rn(order(unpack(stage_word(st, 1, q))), bias2);
         float2 dl = softplus ? softplus2<FAST>(raw) : raw;
         dl = in ? dl : f2(0.f, 0.f);
-        const float2 du = __fmul2_rn(dl, u);  // zero outside the range: u there is finite box fill or data
+        // the input factor of the state update: Delta u (ZOH: u, the weight being formed per state)
+        const float2 du = zoh ? (in ? u : f2(0.f, 0.f)) : __fmul2_rn(dl, u);  // zero outside the range
         if (pair_owner) du_chan[par * MAX_CH * 4 + ps] = make_float4(dl.x, dl.y, du.x, du.y);
         if (MODE == MODE_STATES && pair_owner) sdt_acc += dl.x + dl.y;
         if (MODE == MODE_FULL) {
             Du = __fmul2_rn(D2, u);
-            if (HAS_Z) g = silu2<FAST>(unpack(stage_word(st, 2, q)));
+            if (HAS_Z) g = silu2<FAST>(order(unpack(stage_word(st, 2, q))));
         }
     };
     // partial sums of this lane's group of 4 lanes (lanes 4 (s / 4) .. + 3 of the channel)
@@ -386,10 +411,13 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         float2 yy = __fadd2_rn(ys, Du);
         if (HAS_Z) yy = __fmul2_rn(yy, g);
         const bool st = pair_owner && (unsigned)r < lenv;
+        // reverse: logical steps tau, tau + 1 (tau = t_begin + r) are physical L - 1 - tau, L - 2 - tau
+        T *const dst = rev ? yrow + (L - 2 - (t_begin + r)) : ylane + r;
+        yy = order(yy);
         if constexpr (Sh::SPLIT)
-            st_f32x2_if(ylane + r, yy, st);
+            st_f32x2_if(dst, yy, st);
         else
-            st_b32_if(ylane + r, pack_bf16x2(yy.x, yy.y), st);
+            st_b32_if(dst, pack_bf16x2(yy.x, yy.y), st);
     };
 
     const uint64_t descA = tc::umma_desc(tc::smem_addr(sA), 128, 256);
@@ -494,9 +522,18 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const float2 x = __fmul2_rn(dl, A2d[j]);
-                        const float2 bu = __fmul2_rn(du, f2(__uint_as_float(bcp[2 * j]), __uint_as_float(bcp[2 * j + 1])));
-                        hh[j].x = fmaf(ex2_approx(x.x), hh[j].y, bu.x);
-                        hh[j].y = fmaf(ex2_approx(x.y), hh[j].x, bu.y);
+                        const float2 Bt = f2(__uint_as_float(bcp[2 * j]), __uint_as_float(bcp[2 * j + 1]));
+                        const float2 e = f2(ex2_approx(x.x), ex2_approx(x.y));
+                        float2 bu;
+                        if constexpr (zoh) {  // du holds u: B_bar u = (e^{Delta A} - 1) / A * B * u
+                            const float2 w = f2(zoh_weight(e.x, x.x, dl.x, invA[j], aZero[j]),
+                                                zoh_weight(e.y, x.y, dl.y, invA[j], aZero[j]));
+                            bu = __fmul2_rn(__fmul2_rn(w, du), Bt);
+                        } else {
+                            bu = __fmul2_rn(du, Bt);
+                        }
+                        hh[j].x = fmaf(e.x, hh[j].y, bu.x);
+                        hh[j].y = fmaf(e.y, hh[j].x, bu.y);
                     }
                     if (MODE == MODE_FULL) {
                         float2 P = __fmul2_rn(f2(__uint_as_float(ccp[0]), __uint_as_float(ccp[1])), hh[0]);
@@ -563,6 +600,71 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         tc::fence_after_sync();
         tc::tmem_dealloc(*taddr_s, Sh::TMEM_COLS);
     }
+}
+
+
+// Launch of one instantiation: grid (ceil(Dch / channels per CTA), Bsz, grid_chunks), W compute warps
+// plus the producer warp, one CTA per SM.
+template <typename T, int MODE, bool HAS_Z, int S, bool CONV = false, int FLAGS = 0>
+cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int grid_chunks,
+                          cudaStream_t st) {
+    using Sh = TmShape<T, MODE, S, CONV>;
+    auto kern = scan_tm_kernel<T, MODE, HAS_Z, S, CONV, FLAGS>;
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) attr_set[dev] = true;
+    }
+    const long long ch = 32LL * warps / S;
+    dim3 grid((unsigned)((a.Dch + ch - 1) / ch), (unsigned)Bsz, (unsigned)grid_chunks);
+    kern<<<grid, 32 * (warps + 1), Sh::SMEM_BYTES, st>>>(a, maps);  // + the producer warp
+    return cudaGetLastError();
+}
+
+template <typename T, int S, int FLAGS = 0>
+cudaError_t launch_tm_s(int mode, const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int gc,
+                        cudaStream_t st) {
+    if (mode == MODE_STATES) return launch_tm_one<T, MODE_STATES, false, S, false, FLAGS>(a, maps, warps, Bsz, gc, st);
+    return a.z != nullptr ? launch_tm_one<T, MODE_FULL, true, S, false, FLAGS>(a, maps, warps, Bsz, gc, st)
+                          : launch_tm_one<T, MODE_FULL, false, S, false, FLAGS>(a, maps, warps, Bsz, gc, st);
+}
+
+// The instantiations that honour the scan flags: the reverse scan (scan_tm_rev.cu) and the exact
+// zero-order hold, forwards or reverse (scan_tm_zoh.cu); dtype 1 = bf16, S lanes per channel.
+cudaError_t launch_tm_rev(int dtype, int S, int mode, const ScanArgs &a, const TmMaps &maps, int warps,
+                          long long Bsz, int gc, cudaStream_t st);
+cudaError_t launch_tm_zoh(int dtype, int S, int mode, const ScanArgs &a, const TmMaps &maps, int warps,
+                          long long Bsz, int gc, cudaStream_t st);
+
+// Instantiate the kernels of one flag variant for every storage type and lane count.
+template <int FL>
+cudaError_t launch_tm_variant(int dtype, int S, int mode, const ScanArgs &a, const TmMaps &maps, int warps,
+                              long long Bsz, int gc, cudaStream_t st) {
+    if (dtype != 1) return launch_tm_s<float, 4, FL>(mode, a, maps, warps, Bsz, gc, st);
+    switch (S) {
+        case 4: return launch_tm_s<bf16_t, 4, FL>(mode, a, maps, warps, Bsz, gc, st);
+        case 8: return launch_tm_s<bf16_t, 8, FL>(mode, a, maps, warps, Bsz, gc, st);
+        default: return launch_tm_s<bf16_t, 16, FL>(mode, a, maps, warps, Bsz, gc, st);
+    }
+}
+
+// Read and clear a device error word (MAMBA_OK, or MAMBA_ERR_DEVICE if the copy fails).
+inline int read_clear_word(const unsigned int &word, unsigned int *v) {
+    unsigned int zero = 0;
+    *v = 0;
+    if (cudaMemcpyFromSymbol(v, word, sizeof(*v)) != cudaSuccess) {
+        cudaGetLastError();
+        return MAMBA_ERR_DEVICE;
+    }
+    if (*v != 0 && cudaMemcpyToSymbol(word, &zero, sizeof(zero)) != cudaSuccess) {
+        cudaGetLastError();
+        return MAMBA_ERR_DEVICE;
+    }
+    return MAMBA_OK;
 }
 
 }  // namespace mamba

@@ -54,6 +54,27 @@ def test_layer_every_element(name):
           f"last_state {eh:.3g} (tol {TOL_STATE})")
 
 
+@pytest.mark.parametrize("flags", [0x1, 0x3])
+def test_layer_with_flags_every_element(flags):
+    """The 130M-shaped layer with the exact zero-order hold, forwards and in reverse time."""
+    import torch
+    name = "mamba130m_b8_d1536_n16_l2048_bf16"
+    x = inputs.make_workload(name)
+    Bsz, Dch, L, N = x.shape
+    t = dev_inputs(x)
+    y = torch.empty_like(t["u"])
+    h = torch.empty((Bsz, Dch, N), dtype=torch.float32, device="cuda")
+    m.mamba_selective_scan_fwd_ex(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["delta_bias"], 1,
+                                  y, h, flags=flags)
+    torch.cuda.synchronize()
+    assert m.mamba_device_error() == 0
+    yr, hr = oracle.selective_scan(x.f64("u"), x.f64("delta"), x.f64("A"), x.f64("B"), x.f64("C"), x.f64("D"),
+                                   x.f64("z"), x.f64("delta_bias"), disc=1, reverse=bool(flags & 0x2))
+    ey = assert_close(to_host_f64(y), yr, TOL_Y["bf16"], f"{name} flags={flags} y")
+    eh = assert_close(h.cpu().numpy().astype(np.float64), hr, TOL_STATE, f"{name} flags={flags} last_state")
+    print(f"{name} flags={flags}: every element, max err ratio y {ey:.3g}, last_state {eh:.3g}")
+
+
 def test_dna_sequence_every_element_in_channel_blocks():
     import torch
     name = "dna_b1_d1536_n16_l1048576_bf16"

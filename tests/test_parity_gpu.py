@@ -320,3 +320,21 @@ def test_bounded_wait_gives_up_and_reports_timeout(monkeypatch):
     monkeypatch.delenv("MAMBA_TEST_WAIT_POLLS")
     ey, eh = check(x, "after an aborted call")
     print(f"after the aborted calls: y err ratio {ey:.3g}, state {eh:.3g}")
+
+
+# ----------------------------------------------------------------------------- flags on the tensor-memory kernel
+
+@pytest.mark.parametrize("case", sorted(FLAG_CASES))
+@pytest.mark.parametrize("io,N", [("bf16", 12), ("bf16", 16), ("bf16", 32), ("bf16", 64), ("f32", 16)])
+@pytest.mark.parametrize("L", [256, 1000])
+def test_flags_tensor_memory_path(case, io, N, L):
+    """16-byte aligned rows (L a multiple of 8): the flagged tensor-memory kernel, direct and chunked, with
+    and without h0; L = 1000 ends in a partial 32-step tile."""
+    flags, disc, rev = FLAG_CASES[case]
+    x = inputs.make_scan_inputs(2, 40, N, L, io=io, seed=100 + N + L)
+    h0 = np.random.default_rng(N + L).normal(0, 0.3, (2, 40, N)).astype(np.float32)
+    for h, chunk_len in ((None, -1), (h0, -1), (h0, 128)):
+        yg, hg = run_gpu(x, h0=h, flags=flags, chunk_len=chunk_len)
+        yr, hr = run_oracle(x, h0=None if h is None else h.astype(np.float64), disc=disc, reverse=rev)
+        assert_close(yg, yr, TOL_Y[io], f"{case} N={N} L={L} {io} chunk={chunk_len} y")
+        assert_close(hg, hr, TOL_STATE, f"{case} N={N} L={L} {io} chunk={chunk_len} last_state")
