@@ -109,13 +109,25 @@ int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A, c
  *   h0          [Bsz][Dch][N] fp32 initial state (NULL = zero).  With
  *               MAMBA_FLAG_REVERSE it is the state "after" t = L, i.e. the
  *               state the backward-in-time scan starts from.
- *   flags       MAMBA_FLAG_ZOH | MAMBA_FLAG_REVERSE (0 = plain forward scan);
- *               a call with flags runs the general scalar-load kernel, which is
- *               slower than the plain forward scan's kernels
+ *   flags       MAMBA_FLAG_ZOH | MAMBA_FLAG_REVERSE (0 = plain forward scan).
+ *               With 16-byte aligned rows and 8 < N <= 64 (fp32: N <= 16) a
+ *               flagged call runs on the tensor-memory kernel like a plain
+ *               one; otherwise on the general scalar-load kernel (slower).
  *   chunk_len   0: automatic choice between the direct and the chunked scan;
  *               > 0: force the chunked scan with chunks of this many steps
  *                    (rounded up to the kernel's time tile);
  *               < 0: force the direct (single pass) scan.
+ *               The chunked scan is the two-pass one (chunk end states from a
+ *               zero state, the carry, every chunk again from its entering
+ *               state).  With the environment variable
+ *               MAMBA_CHUNKED_SCAN=truncated (read on every call) a call
+ *               without flags, aligned, 8 < N <= 64, chunk_len a multiple of
+ *               32 and no convolution runs the decay-truncated scan instead:
+ *               every chunk once from a zero state (y, end state), the carry,
+ *               then y += the entering state's contribution, decayed with no
+ *               input, up to where it falls below 2^-40 of that state (only
+ *               when the decay is monotone: softplus on, every A <= 0).  It is
+ *               faster only when every channel's steps are large.
  *   workspace, workspace_bytes
  *               caller-owned device scratch for the chunked scan (256-byte
  *               aligned, at least mamba_scan_workspace_size(...) bytes), or

@@ -211,23 +211,12 @@ int scan_impl(const void *u, const void *delta, const float *A, const void *B, c
     a.chunk_len = plan.chunk_len;
     a.nchunks = plan.K;
     int rc = MAMBA_OK;
-    // pass A over chunks 0..K-2 (the last chunk's end state is produced by pass B)
-    a.hin = nullptr;
-    a.ws_h = ws_h;
-    a.ws_sdt = ws_sdt;
-    const cudaError_t ea = launch_scan(dtype, MODE_STATES, vec, a, Bsz, plan.K - 1, stream);
-    if (ea == cudaErrorNotSupported && conv_w != nullptr) {  // nothing launched yet
+    const cudaError_t e = run_chunked(dtype, vec, a, Bsz, ws_h, ws_sdt, h0, stream);
+    if (e == cudaErrorNotSupported && conv_w != nullptr) {  // nothing launched yet
         if (owned) cudaFreeAsync(ws, stream);
         return kNotFused;
     }
-    if (ea != cudaSuccess) rc = MAMBA_ERR_LAUNCH;
-    if (rc == MAMBA_OK && launch_carry(A, h0, ws_h, ws_sdt, Bsz, Dch, N, plan.K, stream) != cudaSuccess)
-        rc = MAMBA_ERR_LAUNCH;
-    a.hin = ws_h;
-    a.ws_h = nullptr;
-    a.ws_sdt = nullptr;
-    if (rc == MAMBA_OK && launch_scan(dtype, MODE_FULL, vec, a, Bsz, plan.K, stream) != cudaSuccess)
-        rc = MAMBA_ERR_LAUNCH;
+    if (e != cudaSuccess) rc = MAMBA_ERR_LAUNCH;
     if (owned && cudaFreeAsync(ws, stream) != cudaSuccess) {
         cudaGetLastError();
         if (rc == MAMBA_OK) rc = MAMBA_ERR_LAUNCH;

@@ -42,16 +42,30 @@ cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long l
 cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &a, long long Bsz, int grid_chunks, cudaStream_t st);
 
 // Carry pass of the chunked scan: per (b, d, n) an exclusive combine over the
-// K chunk (decay, end-state) pairs; writes every chunk's initial state into
-// ws_h in place (hin[k] = prod decay * h0 + ...).
+// chunk (decay, end-state) pairs; writes every chunk's initial state into ws_h
+// in place (hin[k] = prod decay * h0 + ...).  all_chunks false: ws_h and
+// ws_sdt hold chunks 0..K-2 (the two-pass scan).  True: they hold all K chunks
+// (the decay-truncated scan) and the state after the last chunk goes to
+// last_state (if not null).
 cudaError_t launch_carry(const float *A, const float *h0, float *ws_h, const float *ws_sdt, long long Bsz,
-                         long long Dch, long long N, int K, cudaStream_t st);
+                         long long Dch, long long N, int K, cudaStream_t st, bool all_chunks = false,
+                         float *last_state = nullptr);
+
+// Whether the decay-truncated chunked scan (tensor-memory kernel) serves these sizes and flags.
+bool tm_chunked_for(int dtype, long long N, int flags, bool vec, bool conv);
+
+// The chunked scan after its workspace is in hand: the decay-truncated scan where it is requested
+// (MAMBA_CHUNKED_SCAN=truncated) and tm_chunked_for holds, else the two-pass scan (chunk end states, carry, seeded rescan).  a.chunk_len and a.nchunks
+// set; ws_h [Bsz][K][Dch][N] and ws_sdt [Bsz][K][Dch]; h0 may be null.
+cudaError_t run_chunked(int dtype, bool vec, ScanArgs a, long long Bsz, float *ws_h, float *ws_sdt,
+                        const float *h0, cudaStream_t st);
 
 // Read and clear the device error words of the tensor-memory scan's translation units (its plain, reverse
 // and zero-order-hold instantiations); MAMBA_OK or MAMBA_ERR_DEVICE.
 int tm_read_clear_error(unsigned int *v);
 int tm_rev_read_clear_error(unsigned int *v);
 int tm_zoh_read_clear_error(unsigned int *v);
+int tm_chunk_read_clear_error(unsigned int *v);
 
 struct StepArgs {
     float *state;

@@ -106,20 +106,13 @@ extern "C" int mamba_selective_scan_fwd_noalloc(const void *u, const void *delta
     void *scratch = nullptr;
     const int rc = scratch_address(&scratch);
     if (rc != MAMBA_OK) return rc;
-    // Pass A writes every (chunk < K-1) end state and step sum before the carry
-    // reads it, and the carry writes every chunk's initial state before pass B
-    // reads it, so the stale contents of earlier calls are never read.
+    // The first pass writes every chunk end state and step sum it covers before
+    // the carry reads them, and the carry writes every chunk's initial state
+    // before the last pass reads it, so the stale contents of earlier calls are
+    // never read.
     float *ws_h = reinterpret_cast<float *>(scratch);
     float *ws_sdt = reinterpret_cast<float *>(reinterpret_cast<unsigned char *>(scratch) + h_bytes);
     a.chunk_len = cl;
     a.nchunks = (int)K;
-    a.hin = nullptr;
-    a.ws_h = ws_h;
-    a.ws_sdt = ws_sdt;
-    if (launch_scan(dtype, MODE_STATES, vec, a, Bsz, (int)K - 1, st) != cudaSuccess) return MAMBA_ERR_LAUNCH;
-    if (launch_carry(A, h0, ws_h, ws_sdt, Bsz, Dch, N, (int)K, st) != cudaSuccess) return MAMBA_ERR_LAUNCH;
-    a.hin = ws_h;
-    a.ws_h = nullptr;
-    a.ws_sdt = nullptr;
-    return launch_scan(dtype, MODE_FULL, vec, a, Bsz, (int)K, st) == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+    return run_chunked(dtype, vec, a, Bsz, ws_h, ws_sdt, h0, st) == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
 }

@@ -111,4 +111,54 @@ cudaError_t launch_scan(int dtype, int mode, bool vec, const ScanArgs &a, long l
                       : launch_t<float>(mode, vec, a, Bsz, grid_chunks, st);
 }
 
+bool tm_chunked_for(int dtype, long long N, int flags, bool vec, bool conv) {
+    return vec && !conv && flags == 0 && tm_kernel_for(dtype, N);
+}
+
+// MAMBA_CHUNKED_SCAN=truncated selects the decay-truncated chunked scan (read on every call).  It
+// pays off only where every channel's state decays within a small part of a chunk (large steps):
+// with the Mamba step initialisation (dt log-uniform in [1e-3, 1e-1], A_n = -n) a channel with
+// dt near 1e-3 keeps its entering state for more than ten thousand steps, the correction runs
+// to the end of nearly every chunk and costs more than the states-only pass it replaces.
+static bool decay_truncated_requested() {
+    const char *v = std::getenv("MAMBA_CHUNKED_SCAN");
+    return v != nullptr && std::strcmp(v, "truncated") == 0;
+}
+
+cudaError_t run_chunked(int dtype, bool vec, ScanArgs a, long long Bsz, float *ws_h, float *ws_sdt,
+                        const float *h0, cudaStream_t st) {
+    const int K = a.nchunks;
+    a.ws_h = ws_h;
+    a.ws_sdt = ws_sdt;
+    if (decay_truncated_requested() && tm_chunked_for(dtype, a.N, a.flags, vec, a.conv_w != nullptr) &&
+        a.chunk_len % 32 == 0) {
+        // Decay-truncated scan: (1) every chunk from a zero state -- y, end state and sum of Delta;
+        // (2) the carry -- the state entering each chunk, and the final state; (3) y += the
+        // contribution of each chunk's entering state, decaying with no input, as far as it matters.
+        // Chunk 0 enters with h0 (zero when none is given: no correction there).
+        a.hin = nullptr;
+        a.chunk0 = 0;
+        cudaError_t e = launch_scan_tm(dtype, MODE_FULL_STATES, a, Bsz, K, st);
+        if (e != cudaErrorNotSupported) {  // NotSupported: nothing launched, the two-pass scan serves it
+            if (e == cudaSuccess) e = launch_carry(a.A, h0, ws_h, ws_sdt, Bsz, a.Dch, a.N, K, st, true, a.last_state);
+            a.hin = ws_h;
+            a.ws_h = nullptr;
+            a.ws_sdt = nullptr;
+            a.chunk0 = h0 != nullptr ? 0 : 1;
+            if (e == cudaSuccess && K > a.chunk0) e = launch_scan_tm(dtype, MODE_CORR, a, Bsz, K - a.chunk0, st);
+            return e;
+        }
+    }
+    // two-pass scan: (A) chunks 0..K-2 from zero -- end state and sum of Delta; the carry; (B) every chunk
+    // again from its entering state
+    a.hin = nullptr;
+    cudaError_t e = launch_scan(dtype, MODE_STATES, vec, a, Bsz, K - 1, st);
+    if (e != cudaSuccess) return e;
+    if ((e = launch_carry(a.A, h0, ws_h, ws_sdt, Bsz, a.Dch, a.N, K, st)) != cudaSuccess) return e;
+    a.hin = ws_h;
+    a.ws_h = nullptr;
+    a.ws_sdt = nullptr;
+    return launch_scan(dtype, MODE_FULL, vec, a, Bsz, K, st);
+}
+
 }  // namespace mamba

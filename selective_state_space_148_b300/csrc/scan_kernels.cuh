@@ -35,7 +35,11 @@
 
 namespace mamba {
 
-enum { MODE_FULL = 0, MODE_STATES = 1 };
+// MODE_FULL: y (and last_state) of a chunk from its initial state.  MODE_STATES: a chunk's end state
+// from zero and its sum of Delta (no y).  The tensor-memory kernel also has MODE_FULL_STATES (y from a
+// zero initial state and the end state and sum of Delta) and MODE_CORR (y += the contribution of the
+// chunk's entering state, decaying with no input), the two passes of the decay-truncated chunked scan.
+enum { MODE_FULL = 0, MODE_STATES = 1, MODE_FULL_STATES = 2, MODE_CORR = 3 };
 
 struct ScanArgs {
     const void *u, *delta, *z, *Bm, *Cm;
@@ -57,6 +61,7 @@ struct ScanArgs {
     // non-null: `u` holds x and u = SiLU(causal width-4 conv of x) is formed in
     // the kernel (tensor-memory kernel only): taps [Dch][4], bias [Dch] or null
     const float *conv_w, *conv_b;
+    int chunk0;  // MODE_CORR: chunk of blockIdx.z == 0
 };
 
 enum { SCAN_FLAG_ZOH = 1, SCAN_FLAG_REVERSE = 2 };

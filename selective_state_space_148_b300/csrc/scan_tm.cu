@@ -132,6 +132,10 @@ cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &args, long long 
                     encode_3d(&maps.B, a.Bm, bf16, a.L, a.N, Bsz, 4u * S, false) &&
                     encode_3d(&maps.C, a.Cm, bf16, a.L, a.N, Bsz, 4u * S, false);
     if (!ok) return cudaErrorNotSupported;
+    if (mode == MODE_FULL_STATES || mode == MODE_CORR) {
+        if (conv || a.flags != 0) return cudaErrorNotSupported;
+        return launch_tm_chunk(dtype, S, mode, a, maps, warps, Bsz, grid_chunks, st);
+    }
     if (a.flags & SCAN_FLAG_ZOH) return launch_tm_zoh(dtype, S, mode, a, maps, warps, Bsz, grid_chunks, st);
     if (a.flags & SCAN_FLAG_REVERSE) return launch_tm_rev(dtype, S, mode, a, maps, warps, Bsz, grid_chunks, st);
     if (conv)
@@ -153,9 +157,9 @@ int tm_read_clear_error(unsigned int *v) { return read_clear_word(g_device_error
 }  // namespace mamba
 
 extern "C" int mamba_device_error(void) {
-    unsigned int v = 0, r = 0, z = 0;
+    unsigned int v = 0, r = 0, z = 0, c = 0;
     if (mamba::tm_read_clear_error(&v) != MAMBA_OK || mamba::tm_rev_read_clear_error(&r) != MAMBA_OK ||
-        mamba::tm_zoh_read_clear_error(&z) != MAMBA_OK)
+        mamba::tm_zoh_read_clear_error(&z) != MAMBA_OK || mamba::tm_chunk_read_clear_error(&c) != MAMBA_OK)
         return MAMBA_ERR_DEVICE;
-    return (v | r | z) != 0 ? MAMBA_ERR_DEVICE_TIMEOUT : MAMBA_OK;
+    return (v | r | z | c) != 0 ? MAMBA_ERR_DEVICE_TIMEOUT : MAMBA_OK;
 }

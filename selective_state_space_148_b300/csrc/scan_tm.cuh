@@ -116,8 +116,10 @@ struct TmShape {
     static constexpr int OFF_X = OFF_A + A_BYTES;
     static constexpr int OFF_DU = OFF_X + 2 * X_BYTES;
     static constexpr int OFF_P = OFF_DU + 2 * DU_BYTES;
-    static constexpr int OFF_BAR = OFF_P + (MODE == MODE_FULL ? 2 * P_BYTES : 0);
-    static constexpr int SMEM_BYTES = OFF_BAR + 128 + 1024;  // + room to align the base to 1024 bytes
+    static constexpr int OFF_BAR = OFF_P + (MODE != MODE_STATES ? 2 * P_BYTES : 0);
+    static constexpr int OFF_VOTE = OFF_BAR + 128;  // MODE_CORR: super-tile at which each compute warp's
+                                                    // states had decayed below the stopping bound
+    static constexpr int SMEM_BYTES = OFF_VOTE + 4 * MAX_WARPS + 1024;  // + room to align the base to 1024 bytes
     static_assert(5 + NST <= 8, "full[2], empty[2], done and io[NST] in the first 64 bytes of the barrier block");
     static_assert(IO_TILE % 1024 == 0 && BC_TILE % 1024 == 0, "swizzled boxes need 1024-byte aligned tiles");
     static_assert(SWZ == 4 || SWZ == 8, "rows of 64 or 128 bytes");
@@ -139,6 +141,9 @@ __global__ void __launch_bounds__(TmShape<T, MODE, S_, CONV>::LAUNCH_THR, 1)
 scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     using Sh = TmShape<T, MODE, S_, CONV>;
     constexpr bool FAST = sizeof(T) == 2;
+    constexpr bool HASY = MODE != MODE_STATES;                             // forms y (and reads C)
+    constexpr bool ENDS = MODE == MODE_STATES || MODE == MODE_FULL_STATES;  // writes end states, sum of Delta
+    constexpr bool CORR = MODE == MODE_CORR;
     constexpr int S = Sh::S, TT = Sh::TT, TB = Sh::TB, NSUB = Sh::NSUB, COLS = Sh::COLS, MAX_CH = Sh::MAX_CH;
     constexpr int NST = Sh::NST;
     constexpr uint32_t kWaitPolls = 1u << 24;  // drain waits before TMEM and shared memory are released
@@ -157,6 +162,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     uint64_t *const done = full + 4;   // abort path: all MMAs done
     uint64_t *const io = full + 5;     // [NST] stage loads landed
     uint32_t *const taddr_s = reinterpret_cast<uint32_t *>(smem + Sh::OFF_BAR + 64);
+    volatile int *const first_small = reinterpret_cast<volatile int *>(smem + Sh::OFF_VOTE);  // [MAX_WARPS]
     volatile int *const abort_flag = reinterpret_cast<volatile int *>(smem + Sh::OFF_BAR + 68);
 
     const int nthr = blockDim.x, ncw = nthr / 32 - 1, ch = 32 * ncw / S;  // compute warps, channels of this CTA
@@ -172,7 +178,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     const long long d = d0 + c;
     const bool valid = !producer && d < a.Dch;
     const long long b = blockIdx.y;
-    const int kch = blockIdx.z;
+    const int kch = blockIdx.z + (CORR ? a.chunk0 : 0);
     const long long N = a.N, L = a.L;
     const long long t_begin = (long long)kch * a.chunk_len;
     const int len = (int)(min(L, t_begin + a.chunk_len) - t_begin);  // steps of this chunk (< 2^31)
@@ -202,6 +208,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         tc::mbar_init(done, 1);
         for (int k = 0; k < NST; ++k) tc::mbar_init(&io[k], 1);
         *abort_flag = 0;
+        for (int w = 0; w < Sh::MAX_WARPS; ++w) first_small[w] = 0x7fffffff;
         tc::fence_mbar_init();
     }
 
@@ -225,7 +232,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     }
     // FL_REV is launched only for reverse scans; FL_ZOH serves both directions
     const bool rev = FLAGS == FL_REV || (FLAGS == FL_ZOH && (a.flags & SCAN_FLAG_REVERSE) != 0);
-    const float Dd = (a.D != nullptr && valid) ? a.D[dd] : 0.f;
+    const float Dd = (a.D != nullptr && valid && !CORR) ? a.D[dd] : 0.f;  // the correction has no input
     const float bias = (a.bias != nullptr && valid) ? a.bias[dd] : 0.f;
     const float2 bias2 = f2(bias, bias);
     const float2 D2 = f2(Dd, Dd);
@@ -287,7 +294,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         unsigned char *xbase = sX + xb * Sh::X_BYTES;
         for (int n = lane; n < COLS; n += 32) {
             int t, which, col;
-            if constexpr (MODE == MODE_FULL) {
+            if constexpr (HASY) {
                 const int j = n & 15;
                 t = 2 * (n >> 4) + (j & 1);
                 which = j >> 3;
@@ -387,10 +394,11 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         float2 dl = softplus ? softplus2<FAST>(raw) : raw;
         dl = in ? dl : f2(0.f, 0.f);
         // the input factor of the state update: Delta u (ZOH: u, the weight being formed per state)
-        const float2 du = zoh ? (in ? u : f2(0.f, 0.f)) : __fmul2_rn(dl, u);  // zero outside the range
+        // (the correction pass carries the entering state only: no input)
+        const float2 du = CORR ? f2(0.f, 0.f) : zoh ? (in ? u : f2(0.f, 0.f)) : __fmul2_rn(dl, u);
         if (pair_owner) du_chan[par * MAX_CH * 4 + ps] = make_float4(dl.x, dl.y, du.x, du.y);
-        if (MODE == MODE_STATES && pair_owner) sdt_acc += dl.x + dl.y;
-        if (MODE == MODE_FULL) {
+        if (ENDS && pair_owner) sdt_acc += dl.x + dl.y;
+        if (HASY) {
             Du = __fmul2_rn(D2, u);
             if (HAS_Z) g = silu2<FAST>(order(unpack(stage_word(st, 2, q))));
         }
@@ -400,7 +408,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     // y of this lane's pair at offset r from the channel's S partial sums: each lane adds its group's
     // 4 partials, the S / 4 groups are combined with shuffles
     auto output_pair = [&](int r, int par, float2 Du, float2 g) {
-        if (MODE != MODE_FULL) return;
+        if (!HASY) return;
         const float *pp = p_chan + par * Sh::MAX_THR * Sh::P_STRIDE;
         float2 ys = *reinterpret_cast<const float2 *>(pp);
 #pragma unroll
@@ -414,6 +422,16 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         // reverse: logical steps tau, tau + 1 (tau = t_begin + r) are physical L - 1 - tau, L - 2 - tau
         T *const dst = rev ? yrow + (L - 2 - (t_begin + r)) : ylane + r;
         yy = order(yy);
+        if constexpr (CORR) {  // y += the entering state's contribution
+            if constexpr (Sh::SPLIT) {
+                if (st) yy = __fadd2_rn(yy, *reinterpret_cast<const float2 *>(dst));
+            } else {
+                if (st) {
+                    const uint32_t w = *reinterpret_cast<const uint32_t *>(dst);
+                    yy = __fadd2_rn(yy, f2(bf16_lo(w), bf16_hi(w)));
+                }
+            }
+        }
         if constexpr (Sh::SPLIT)
             st_f32x2_if(dst, yy, st);
         else
@@ -437,6 +455,25 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     const uint32_t tmem_lane = *taddr_s + (static_cast<uint32_t>((warp & 3) * 32) << 16);
     int last_loaded = -1;  // producer lane 0: latest super-tile whose loads were issued
     int mma_issued = 0;    // producer lane 0: MMAs issued
+    bool stopped = false;  // producer: MODE_CORR stopped before the end of the chunk
+    // MODE_CORR: stop at super-tile sup once every compute warp's states had decayed by the end of
+    // super-tile sup - 2 (the same answer for every warp: entries up to sup - 2 are final)
+    auto corr_done = [&](int sup) {
+        int m = lane < ncw ? first_small[lane] : 0;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, off));
+        return m <= sup - 2;
+    };
+    // MODE_CORR: the bound below which a state's contribution is dropped, and whether its decay is monotone
+    float thr[CORR ? 4 : 1];
+    bool monotone = CORR && softplus;
+    if constexpr (CORR) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            thr[j] = fabsf(hh[j].y) * 0x1p-40f;
+            monotone = monotone && A2d[j].x <= 0.f;
+        }
+    }
     if (producer) {
         if (lane == 0)
             for (int sn = 0; sn < NST && sn < nsup; ++sn) {
@@ -452,6 +489,10 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                 ok = __all_sync(0xffffffffu, wait_or_abort(&empty[sn & 1], ((sn - 2) >> 1) & 1, true));
             if (!ok) {
                 *abort_flag = 1;
+                break;
+            }
+            if (CORR && sn >= 2 && corr_done(sn)) {  // the compute warps stop at the same super-tile
+                stopped = true;
                 break;
             }
             tc::fence_after_sync();
@@ -477,8 +518,19 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         __syncwarp();
 
         int k_cur = 0;  // stage of super-tile sup
+        int last_sup = nsup - 1;  // the last super-tile processed
+        bool recorded = false;    // MODE_CORR: this warp's decay point is in first_small
         for (int sup = 0; sup < nsup; ++sup) {
             const int k_nxt = k_cur == NST - 1 ? 0 : k_cur + 1;
+            if (CORR && sup >= 2) {
+                // every compute warp is done with super-tile sup - 2 (the producer waited for that before
+                // the MMA of sup); this acquire makes their first_small entries visible
+                if (!__all_sync(0xffffffffu, wait_or_abort(&empty[sup & 1], ((sup - 2) >> 1) & 1, false))) *abort_flag = 1;
+                if (corr_done(sup)) {
+                    last_sup = sup - 1;
+                    break;
+                }
+            }
             // this super-tile's B/C are in TMEM buffer sup & 1 (after an abort the
             // loads below still read allocated TMEM; the results are then discarded)
             if (!__all_sync(0xffffffffu, wait_or_abort(&full[sup & 1], (sup >> 1) & 1, false))) *abort_flag = 1;
@@ -492,7 +544,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                 // MODE_STATES: B of the 4 step pairs in bcu[0] (8 columns each), no C
                 uint32_t bcu[2][32];
                 tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64, bcu[0]);
-                if constexpr (MODE == MODE_FULL) {
+                if constexpr (HASY) {
                     tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64 + 32, bcu[1]);
                     tc::tmem_wait_ld_tied(bcu[0], bcu[1]);
                 } else {
@@ -517,7 +569,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                 for (int p = 0; p < TB / 2; ++p) {
                     const float2 dl = f2(dq[p].x, dq[p].y);
                     const float2 du = f2(dq[p].z, dq[p].w);
-                    const uint32_t *bcp = MODE == MODE_FULL ? bcu[p >> 1] + 16 * (p & 1) : bcu[0] + 8 * p;
+                    const uint32_t *bcp = HASY ? bcu[p >> 1] + 16 * (p & 1) : bcu[0] + 8 * p;
                     const uint32_t *ccp = bcp + 8;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -535,7 +587,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                         hh[j].x = fmaf(e.x, hh[j].y, bu.x);
                         hh[j].y = fmaf(e.y, hh[j].x, bu.y);
                     }
-                    if (MODE == MODE_FULL) {
+                    if (HASY) {
                         float2 P = __fmul2_rn(f2(__uint_as_float(ccp[0]), __uint_as_float(ccp[1])), hh[0]);
                         P = __ffma2_rn(f2(__uint_as_float(ccp[2]), __uint_as_float(ccp[3])), hh[1], P);
                         P = __ffma2_rn(f2(__uint_as_float(ccp[4]), __uint_as_float(ccp[5])), hh[2], P);
@@ -544,12 +596,25 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                         pq[2 * p + 1] = P.y;
                     }
                 }
-                if (MODE == MODE_FULL) {
+                if (HASY) {
                     float *prow = sP + ((q & 1) * Sh::MAX_THR + tid) * Sh::P_STRIDE;
                     *reinterpret_cast<float4 *>(prow) = make_float4(pq[0], pq[1], pq[2], pq[3]);
                     *reinterpret_cast<float4 *>(prow + 4) = make_float4(pq[4], pq[5], pq[6], pq[7]);
                 }
                 __syncwarp();  // partials of sub-tile i and Delta of sub-tile i+1 visible to the channel's lanes
+            }
+            if constexpr (CORR) {
+                // Once every state of the warp has decayed below 2^-40 of the state it entered the chunk
+                // with, it stays there (softplus Delta > 0 and A <= 0: each step multiplies it by
+                // exp(Delta A) <= 1), and what it adds to y is below fp32 resolution of the carried
+                // contribution: record the super-tile, once.
+                bool small = monotone;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) small = small && fabsf(hh[j].y) <= thr[j];
+                if (__all_sync(0xffffffffu, small) && !recorded) {
+                    if (lane == 0) first_small[warp] = sup;
+                    recorded = true;
+                }
             }
             // this warp is done with TMEM buffer sup & 1 and with the stage of sup
             tc::fence_before_sync();
@@ -558,8 +623,8 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
             k_cur = k_nxt;
         }
 
-        output_pair((nsup - 1) * TT + 3 * TB + 2 * ps, 1, Du_r[1], g_r[1]);  // the last sub-tile is odd
-        if (MODE == MODE_STATES) {
+        output_pair(last_sup * TT + 3 * TB + 2 * ps, 1, Du_r[1], g_r[1]);  // the last sub-tile is odd
+        if (ENDS) {
             float sdt = sdt_acc;
 #pragma unroll
             for (int off = 1; off < S; off <<= 1) sdt += __shfl_xor_sync(0xffffffffu, sdt, off);
@@ -572,7 +637,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                 }
                 if (s == 0) a.ws_sdt[base] = sdt;
             }
-        } else if (a.last_state != nullptr && valid && kch == a.nchunks - 1) {
+        } else if (MODE == MODE_FULL && a.last_state != nullptr && valid && kch == a.nchunks - 1) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const long long n = 4LL * s + j;
@@ -583,8 +648,8 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
 
     tc::fence_before_sync();
     __syncthreads();
-    if (producer && lane == 0 && *abort_flag != 0) {
-        atomicOr(&g_device_error, 1u);
+    if (producer && lane == 0 && *abort_flag != 0) atomicOr(&g_device_error, 1u);
+    if (producer && lane == 0 && (*abort_flag != 0 || stopped)) {
         // the MMAs and loads this CTA started must finish before its TMEM and
         // shared memory are released (each stage has at most its latest
         // issued phase open)
@@ -632,6 +697,10 @@ cudaError_t launch_tm_s(int mode, const ScanArgs &a, const TmMaps &maps, int war
     return a.z != nullptr ? launch_tm_one<T, MODE_FULL, true, S, false, FLAGS>(a, maps, warps, Bsz, gc, st)
                           : launch_tm_one<T, MODE_FULL, false, S, false, FLAGS>(a, maps, warps, Bsz, gc, st);
 }
+
+// The two passes of the decay-truncated chunked scan (scan_tm_chunk.cu): MODE_FULL_STATES and MODE_CORR.
+cudaError_t launch_tm_chunk(int dtype, int S, int mode, const ScanArgs &a, const TmMaps &maps, int warps,
+                            long long Bsz, int gc, cudaStream_t st);
 
 // The instantiations that honour the scan flags: the reverse scan (scan_tm_rev.cu) and the exact
 // zero-order hold, forwards or reverse (scan_tm_zoh.cu); dtype 1 = bf16, S lanes per channel.

@@ -338,3 +338,33 @@ def test_flags_tensor_memory_path(case, io, N, L):
         yr, hr = run_oracle(x, h0=None if h is None else h.astype(np.float64), disc=disc, reverse=rev)
         assert_close(yg, yr, TOL_Y[io], f"{case} N={N} L={L} {io} chunk={chunk_len} y")
         assert_close(hg, hr, TOL_STATE, f"{case} N={N} L={L} {io} chunk={chunk_len} last_state")
+
+
+# ----------------------------------------------------------------------------- decay-truncated chunked scan
+
+@pytest.mark.parametrize("regime", ["fast_decay", "slow_decay", "no_softplus", "growing_state"])
+@pytest.mark.parametrize("io", ["bf16", "f32"])
+def test_chunked_scan_correction_regimes(regime, io, monkeypatch):
+    """The decay-truncated chunked scan (MAMBA_CHUNKED_SCAN=truncated) corrects each chunk's y for its
+    entering state and stops where that contribution has decayed below fp32 resolution: a stop after a
+    few tiles (dt near 1), no stop within a 1024-step chunk (dt near 1e-3, the smallest step of the
+    workloads), and the cases where the decay is not guaranteed monotone (softplus off; a positive A)
+    and the correction must run to the end of every chunk.  With and without h0."""
+    monkeypatch.setenv("MAMBA_CHUNKED_SCAN", "truncated")
+    x = inputs.make_scan_inputs(1, 40, 16, 6144, io=io, seed=120)
+    softplus = regime != "no_softplus"
+    if regime == "fast_decay":
+        x.delta_bias = np.full(40, 1.0, dtype=np.float32)        # dt = softplus(1 + N(0, 0.5)) ~ 1.3
+    elif regime == "slow_decay":
+        x.delta_bias = np.full(40, -6.9, dtype=np.float32)       # dt ~ 1e-3
+    elif regime == "no_softplus":
+        x.delta_bias = np.full(40, 2.0, dtype=np.float32)        # Delta = raw + 2 > 0 in practice
+    else:
+        x.A = x.A.copy()
+        x.A[:, 0] = 0.02                                         # one growing state per channel
+    h0 = np.random.default_rng(3).normal(0, 0.3, (1, 40, 16)).astype(np.float32)
+    for h in (None, h0):
+        yg, hg = run_gpu(x, softplus=softplus, h0=h, chunk_len=1024)
+        yr, hr = run_oracle(x, softplus=softplus, h0=None if h is None else h.astype(np.float64))
+        assert_close(yg, yr, TOL_Y[io], f"{regime} {io} h0={h is not None} y")
+        assert_close(hg, hr, TOL_STATE, f"{regime} {io} last_state")
