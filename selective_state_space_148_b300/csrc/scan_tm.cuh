@@ -216,7 +216,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     // hh[j] = (h_n(t), h_n(t+1)) of the last step pair, .y the current state.
     float2 A2d[4], hh[4];
     constexpr bool zoh = FLAGS == FL_ZOH;
-    float invA[zoh ? 4 : 1], aZero[zoh ? 4 : 1];  // ZOH: 1/A_n (0 where A_n = 0) and [A_n = 0]
+    float invA[zoh ? 4 : 1];  // ZOH: 1/A_n (0 where A_n = 0)
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const long long n = 4LL * s + j;
@@ -225,10 +225,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
         if (a.hin != nullptr && valid && n < N) hn = a.hin[((b * a.nchunks + kch) * a.Dch + dd) * N + n];
         A2d[j] = f2(an, an);
         hh[j] = f2(0.f, hn);
-        if constexpr (zoh) {
-            invA[j] = an != 0.f ? kLog2e / an : 0.f;
-            aZero[j] = an == 0.f ? 1.f : 0.f;
-        }
+        if constexpr (zoh) invA[j] = an != 0.f ? kLog2e / an : 0.f;
     }
     // FL_REV is launched only for reverse scans; FL_ZOH serves both directions
     const bool rev = FLAGS == FL_REV || (FLAGS == FL_ZOH && (a.flags & SCAN_FLAG_REVERSE) != 0);
@@ -578,9 +575,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                         const float2 e = f2(ex2_approx(x.x), ex2_approx(x.y));
                         float2 bu;
                         if constexpr (zoh) {  // du holds u: B_bar u = (e^{Delta A} - 1) / A * B * u
-                            const float2 w = f2(zoh_weight(e.x, x.x, dl.x, invA[j], aZero[j]),
-                                                zoh_weight(e.y, x.y, dl.y, invA[j], aZero[j]));
-                            bu = __fmul2_rn(__fmul2_rn(w, du), Bt);
+                            bu = __fmul2_rn(__fmul2_rn(zoh_weight2(e, x, dl, invA[j]), du), Bt);
                         } else {
                             bu = __fmul2_rn(du, Bt);
                         }
