@@ -12,20 +12,26 @@
 //     dDelta_t += dh (B_{t,n} u_t + A_n a h_{t-1}),  dA_n += dh Delta a h_{t-1},  dh *= a
 //   du_t += D dyh,  dD += dyh u_t,  dDelta_raw_t = dDelta_t sigmoid(Delta_raw_t + bias),  dbias += dDelta_raw_t
 //
-// h_{t-1} is needed in reverse order, so states are recomputed by chunks: a
-// forward sweep writes the state at every chunk start (TC steps apart) to a
-// checkpoint workspace; then, chunk by chunk from the end, the chunk's states
-// are recomputed into shared memory from its checkpoint and swept in reverse.
-// Mapping: 4 lanes per channel, NS states per lane (N <= 4 NS), 32 channels
-// per CTA.  Each chunk's inputs (u, Delta_raw, z, dy rows of the CTA's
-// channels, B and C rows) are staged in shared memory with coalesced loads, and
-// its du, ddelta, dz rows leave through shared memory the same way.  B and C
-// are shared by every channel of a batch, so dB and dC are
-// sums over channels: each lane writes its per-step terms to shared memory,
-// the CTA sums them over its 32 channels at the end of a chunk and adds the
-// sums to dB, dC with one atomic add per CTA and element.  dA, dD and dbias
-// (sums over batches and steps) are kept in registers and added atomically at
-// the end.  No device-side waits.
+// One CTA holds 32 channels of one batch row, 4 lanes per channel and NS
+// states per lane, and walks the whole sequence: a forward sweep writes the
+// state at every chunk start (TC = 64 / NS steps apart) to a checkpoint
+// workspace; then, chunk by chunk from the end, the chunk's states are
+// recomputed from its checkpoint into shared memory and swept in reverse.
+//
+// Per chunk, the work that depends only on (channel, step) -- Delta, sigmoid of
+// the Delta pre-activation, the gate and its derivative -- is done once, by the
+// channel's 4 lanes taking TC / 4 steps each, and read back by all 4 lanes from
+// shared memory; those lanes also write the chunk's du, ddelta, dz.  The sums
+// over the 4 lanes of a channel (du, ddelta and yhat for dz) and over the 8
+// channels of a warp (dB, dC) are transposed shuffle reductions: every lane
+// ends with a different total, so no lane waits on a chain of shuffles of one
+// value.  The 4 warps' dB, dC partials are added in shared memory and sent to
+// memory with one vector atomic add per 4 steps.  dA, dD and dbias (sums over
+// batch rows and steps) stay in registers and are added atomically at the end.
+// Steps past L and channels past Dch run as steps with Delta = 0 and dy = 0,
+// which change neither the state nor any gradient, so the sweeps have no
+// per-step branches.  No device-side waits.
+#include <cstdint>
 #include <cstdlib>
 #include <cstring>
 #include <type_traits>
@@ -40,385 +46,478 @@ struct BwdArgs {
     const float *A, *D, *bias;
     void *du, *ddelta, *dz;
     float *dA, *dB, *dC, *dD, *dbias;
-    float *ckpt;  // [Bsz][Dch][K][N]: state before step k * TC
+    float *ckpt;  // [Bsz][Dch][K][NP]: the state before step k * TC
     long long Dch, L, N;
     int softplus;
+    int vec;  // L % 4 == 0 and every row pointer 16-byte aligned: vector loads, stores and atomics
 };
 
-template <typename T, int NS>
-struct BwdShape {
-    static constexpr int S = 4, CH = 32, NTHR = S * CH;
-    static constexpr int TC = 32 / NS;  // steps per chunk: TC * NS = 32 states kept per lane
-    static constexpr int NP = S * NS;   // padded state count
-    // shared memory, floats: recomputed states [TC][NS][NTHR]; the dB, dC terms [TC][NP][CHP] each (channel
-    // innermost, padded to 33 so that the sum over channels reads distinct banks; a term of channel c and
-    // state slice s goes to column (c + ROT s) mod 32, which puts the 32 lanes of a warp's store in 32
-    // banks, and the sum over a row does not depend on the column order); the chunk's inputs u, Delta_raw,
-    // z, dy [4][CH][TCP] and B, C [2][TC][NP]; outputs du, ddelta, dz [3][CH][TCP] (rows padded to TCP =
-    // TC + 1 so that the 8 channels of a warp read distinct banks)
-    static constexpr int CHP = CH + 1, TCP = TC + 1, ROT = (8 - NS) & 31;
-    static constexpr int SH_FLOATS = TC * NS * NTHR, SD_FLOATS = TC * NP * CHP;
-    static constexpr int IN_FLOATS = 4 * CH * TCP, BC_FLOATS = 2 * TC * NP, OUT_FLOATS = 3 * CH * TCP;
-    static_assert(CH == 32, "the column rotation permutes 32 channels");
-    static constexpr size_t SMEM_BYTES =
-        (SH_FLOATS + 2 * SD_FLOATS + IN_FLOATS + BC_FLOATS + OUT_FLOATS) * sizeof(float);
-};
-
-// NS consecutive floats of shared memory (16-byte aligned) into registers with 16-byte loads
 template <int NS>
-__device__ __forceinline__ void load_vec(float (&v)[NS], const float *p) {
+struct BwdShape {
+    static constexpr int S = 4, CH = 32, NTHR = S * CH, NWARP = NTHR / 32;
+    static constexpr int TC = 64 / NS;  // steps per chunk: TC * NS = 64 recomputed states per lane
+    static constexpr int NP = S * NS;   // padded state count
+    static constexpr int G = TC / S;    // steps per lane in the per-(channel, step) work
+    static constexpr int NQ = NS / 4;   // float4 per lane per step of states
+    // shared memory, floats: states [TC][NQ][NTHR] float4 (lane innermost; h, then dh); per (step,
+    // channel) float4s [TC][CH]: {Delta, Delta u, dy g, u}, {sigmoid, dz factor, -, -} and the lane sums
+    // {q, sum_n A_n w_n / ln2, C.h, -}; B, C rows [TC][2][NP]; dB, dC channel sums [TC][2][NP]
+    static constexpr int OFF_H = 0, OFF_R = OFF_H + TC * NS * NTHR, OFF_E = OFF_R + 4 * TC * CH;
+    static constexpr int OFF_Q = OFF_E + 4 * TC * CH, OFF_BC = OFF_Q + 4 * TC * CH;
+    static constexpr int OFF_O = OFF_BC + 2 * TC * NP, FLOATS = OFF_O + 2 * TC * NP;
+    static constexpr size_t SMEM_BYTES = (size_t)FLOATS * sizeof(float);
+    static_assert(2 * NP * (TC / 4) == NTHR, "one thread per (B or C row, 4 steps)");
+    static_assert(NS % 4 == 0 && TC % 4 == 0, "float4 state groups, 4-step row groups");
+    static_assert(TC * NQ == 16 && CH == 32, "channel sums: 128 threads = 16 (step, state quad) x 4 lanes x 2 parities");
+};
+
+// M consecutive elements of storage type T: loaded with one vector access where the caller says the
+// whole group is in range and aligned, element by element (zero past `nvalid`) otherwise.
+template <typename T, int M>
+struct Pack {
+    static constexpr int BYTES = M * (int)sizeof(T), W = BYTES >= 4 ? BYTES / 4 : 1;
+    uint32_t w[W];
+    __device__ __forceinline__ void load(const void *base, long long idx, int nvalid, bool vec) {
+        const T *p = reinterpret_cast<const T *>(base) + idx;
+        if (vec && nvalid >= M && BYTES >= 4) {
+            if constexpr (BYTES == 16) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4 *>(p));
+                w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+            } else if constexpr (BYTES == 8) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
+                w[0] = v.x; w[1] = v.y;
+            } else if constexpr (BYTES == 4) {
+                w[0] = __ldg(reinterpret_cast<const uint32_t *>(p));
+            }
+            return;
+        }
 #pragma unroll
-    for (int k = 0; k < NS; k += 4) {
-        const float4 q = *reinterpret_cast<const float4 *>(p + k);
-        v[k] = q.x;
-        v[k + 1] = q.y;
-        v[k + 2] = q.z;
-        v[k + 3] = q.w;
+        for (int e = 0; e < M; ++e) set(e, e < nvalid ? Io<T>::load(base, idx + e) : 0.f);
+    }
+    __device__ __forceinline__ float get(int e) const {
+        if constexpr (sizeof(T) == 4) return __uint_as_float(w[e]);
+        else return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+    }
+    __device__ __forceinline__ void set(int e, float f) {
+        if constexpr (sizeof(T) == 4) {
+            w[e] = __float_as_uint(f);
+        } else {
+            const uint32_t h = pack_bf16x2(f, 0.f) & 0xffffu;  // round to nearest even
+            w[e >> 1] = (e & 1) ? ((w[e >> 1] & 0x0000ffffu) | (h << 16)) : ((w[e >> 1] & 0xffff0000u) | h);
+        }
+    }
+    __device__ __forceinline__ void store(void *base, long long idx, int nvalid, bool vec) const {
+        T *p = reinterpret_cast<T *>(base) + idx;
+        if (vec && nvalid >= M && BYTES >= 4) {
+            if constexpr (BYTES == 16) *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+            else if constexpr (BYTES == 8) *reinterpret_cast<uint2 *>(p) = make_uint2(w[0], w[1]);
+            else if constexpr (BYTES == 4) *reinterpret_cast<uint32_t *>(p) = w[0];
+            return;
+        }
+#pragma unroll
+        for (int e = 0; e < M; ++e)
+            if (e < nvalid) Io<T>::store(base, idx + e, get(e));
+    }
+};
+
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+// One level of a transposed butterfly: lanes l and l ^ X exchange halves of v[0 .. 2H); afterwards
+// v[0 .. H) holds the pair's sums of the half selected by bit X of the lane (upper half where set).
+template <int H, int X, int V>
+__device__ __forceinline__ void transpose_level(float (&v)[V], int lane) {
+    const bool hi = (lane & X) != 0;
+#pragma unroll
+    for (int k = 0; k < H; ++k) {
+        const float keep = hi ? v[H + k] : v[k], send = hi ? v[k] : v[H + k];
+        v[k] = keep + __shfl_xor_sync(0xffffffffu, send, X);
     }
 }
 
-template <typename T, int NS>
-__global__ void __launch_bounds__(128)
-scan_bwd_kernel(const BwdArgs a, long long K) {
-    using Sh = BwdShape<T, NS>;
-    using IO = Io<T>;
-    constexpr int CH = Sh::CH, NTHR = Sh::NTHR, TC = Sh::TC, NP = Sh::NP;
+template <typename T, int NS, bool HAS_Z>
+__global__ void __launch_bounds__(128, 3)
+scan_bwd_kernel(const BwdArgs a, int K) {
+    using Sh = BwdShape<NS>;
+    constexpr int CH = Sh::CH, NTHR = Sh::NTHR, TC = Sh::TC, NP = Sh::NP, G = Sh::G;
+    constexpr int NQ = Sh::NQ, NH = NS / 2;
     extern __shared__ float4 smem_f4[];
-    float *const sH = reinterpret_cast<float *>(smem_f4);  // [TC][NS][NTHR]
-    float *const sdB = sH + Sh::SH_FLOATS;     // [TC][NP][CHP]
-    float *const sdC = sdB + Sh::SD_FLOATS;
-    float *const sIn = sdC + Sh::SD_FLOATS;    // [4][CH][TC]: u, Delta_raw, z, dy
-    float *const sBC = sIn + Sh::IN_FLOATS;    // [2][TC][NP]: B, C
-    float *const sOut = sBC + Sh::BC_FLOATS;   // [3][CH][TC]: du, ddelta, dz
+    float *const smem = reinterpret_cast<float *>(smem_f4);
+    float4 *const sH = reinterpret_cast<float4 *>(smem + Sh::OFF_H);  // [TC][NQ][NTHR]: h, then dh
+    float4 *const sR = reinterpret_cast<float4 *>(smem + Sh::OFF_R);  // [TC][CH]: Delta, Delta u, dy g, u
+    float4 *const sE = reinterpret_cast<float4 *>(smem + Sh::OFF_E);  // [TC][CH]: sigmoid, dz factor
+    float4 *const sQ = reinterpret_cast<float4 *>(smem + Sh::OFF_Q);  // [TC][CH]: q, wa / ln2, C.h
+    float *const sBC = smem + Sh::OFF_BC;                             // [TC][2][NP]: B, C rows
+    float *const sO = smem + Sh::OFF_O;                               // [TC][2][NP]: dB, dC channel sums
 
-    const int tid = threadIdx.x, s = tid & 3, c = tid >> 2;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, s = tid & 3, c = tid >> 2;
     const long long d = (long long)blockIdx.x * CH + c;
     const bool valid = d < a.Dch;
     const long long dd = valid ? d : 0;
     const long long b = blockIdx.y;
     const long long N = a.N, L = a.L;
-    const long long bc0 = b * N * L;
-    const bool has_z = a.z != nullptr;
+    const bool vec = a.vec != 0;
+    const long long row = (b * a.Dch + dd) * L;  // this channel's (b, d) row of u, Delta, z, dy
+    // B/C rows and dB/dC sums: thread -> (which = B or C, state n, 4-step group rg)
+    const int rg = tid % (TC / 4), rrow = tid / (TC / 4), rwhich = rrow / NP, rn = rrow % NP;
+    const long long bcrow = (b * N + (rn < N ? rn : 0)) * L;
+    // [TC][CH] arrays: the column of channel c at step i is c ^ (2 (i / G mod 4)), so that the 4 lanes
+    // of a channel, which take consecutive groups of G steps, write and read distinct banks
+    auto sw = [&](int i, int cc) { return i * CH + (cc ^ (2 * ((i / G) & 3))); };
 
-    // per-state values in pairs of adjacent states (f32x2 arithmetic)
-    constexpr int NH = NS / 2;
-    float2 Anp[NH], A2p[NH], h2[NH];
-    bool live[NS];
+    // per-state constants in pairs of adjacent states (f32x2): A log2 e
+    float2 A2[NH];
 #pragma unroll
     for (int jp = 0; jp < NH; ++jp) {
         float v[2];
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
-            const int j = 2 * jp + k;
-            const long long n = (long long)s * NS + j;
-            live[j] = valid && n < N;
-            v[k] = live[j] ? a.A[dd * N + n] : 0.f;
+            const long long n = (long long)s * NS + 2 * jp + k;
+            v[k] = (valid && n < N) ? a.A[dd * N + n] * kLog2e : 0.f;
         }
-        Anp[jp] = f2(v[0], v[1]);
-        A2p[jp] = f2(v[0] * kLog2e, v[1] * kLog2e);
-        h2[jp] = f2(0.f, 0.f);
+        A2[jp] = f2(v[0], v[1]);
     }
     const float Dd = (a.D != nullptr && valid) ? a.D[dd] : 0.f;
     const float bias = (a.bias != nullptr && valid) ? a.bias[dd] : 0.f;
-    float *const ck = a.ckpt + ((b * a.Dch + dd) * K) * N + (long long)s * NS;
-    constexpr int TCP = Sh::TCP;
-    const float *const in_u = sIn + c * TCP, *const in_r = sIn + (CH + c) * TCP;
-    const float *const in_z = sIn + (2 * CH + c) * TCP, *const in_dy = sIn + (3 * CH + c) * TCP;
-    const int dcol = (c + Sh::ROT * s) & 31;  // this lane's column in the dB/dC term rows
+    float *const ck = a.ckpt + ((b * a.Dch + dd) * K) * NP + s * NS;
 
-    // Inputs of steps t0 .. t0 + nt - 1 (zero past the end, past Dch, past N): loaded into registers one
-    // chunk ahead (load_chunk), written to shared memory when the chunk starts (store_chunk).  ntens = 2: u
-    // and Delta_raw with B (the forward sweep); 4: also z and dy, with B and C.
-    constexpr int PT = TC, PB = 2;  // elements per thread: 4 * CH * TC / NTHR and 2 * NP * TC / NTHR
-    static_assert(4 * CH * TC == PT * NTHR && 2 * NP * TC == PB * NTHR, "staging splits evenly");
-    float pt[PT], pb[PB];
-    auto load_chunk = [&](long long t0, int nt, int ntens) {
-#pragma unroll
-        for (int r = 0; r < PT; ++r) {
-            const int q = tid + r * NTHR;
-            const int tens = q / (CH * TC), cc = (q / TC) % CH, i = q % TC;
-            const long long dch = (long long)blockIdx.x * CH + cc;
-            const void *p = tens == 0 ? a.u : tens == 1 ? a.delta : tens == 2 ? a.z : a.dy;
-            float v = 0.f;
-            if (tens < ntens && i < nt && dch < a.Dch && p != nullptr) v = IO::load(p, (b * a.Dch + dch) * L + t0 + i);
-            pt[r] = v;
-        }
-#pragma unroll
-        for (int r = 0; r < PB; ++r) {
-            const int q = tid + r * NTHR;
-            const int which = q / (NP * TC), n = (q / TC) % NP, i = q % TC;
-            float v = 0.f;
-            if ((which == 0 || ntens == 4) && i < nt && n < N)
-                v = IO::load(which ? a.Cm : a.Bm, bc0 + (long long)n * L + t0 + i);
-            pb[r] = v;
-        }
+    // this lane's G steps of the chunk starting at t0: how many are in range
+    auto lane_valid = [&](long long t0) {
+        const long long r = L - (t0 + s * G);
+        return valid ? (int)(r < 0 ? 0 : r > G ? G : r) : 0;
     };
-    auto store_chunk = [&]() {
-#pragma unroll
-        for (int r = 0; r < PT; ++r) {
-            const int q = tid + r * NTHR;  // (tensor, channel) row q / TC, step q % TC
-            sIn[(q / TC) * TCP + q % TC] = pt[r];
-        }
-#pragma unroll
-        for (int r = 0; r < PB; ++r) {
-            const int q = tid + r * NTHR;
-            const int which = q / (NP * TC), n = (q / TC) % NP, i = q % TC;
-            sBC[(which * TC + i) * NP + n] = pb[r];
-        }
+    auto row_valid = [&](long long t0) {
+        const long long r = L - (t0 + 4 * rg);
+        return rn < N ? (int)(r < 0 ? 0 : r > 4 ? 4 : r) : 0;
     };
-    auto softplus_of = [&](float raw) { return a.softplus ? softplus_f(raw) : raw; };
+    auto softplus_of = [&](float x) { return a.softplus ? softplus_f(x) : x; };
 
-    auto chunk_len = [&](long long k) { return (int)min((long long)TC, L - k * TC); };
-    // ---- forward sweep: checkpoint the state before every chunk.  It stages FW chunks (TW steps) of u,
-    // Delta_raw and B at a time, one window ahead, in the dB/dC scratch, which is idle until the reverse sweep.
-    constexpr int FW = 4, TW = FW * TC;
-    constexpr int FT = 2 * CH * TW / NTHR, FB = NP * TW / NTHR;  // elements per thread: u/Delta_raw, B
-    static_assert(2 * CH * TW == FT * NTHR && NP * TW == FB * NTHR, "window staging splits evenly");
-    constexpr int TWP = TW + 1;  // padded rows: the 8 channels of a warp read distinct banks
-    static_assert(2 * CH * TWP + NP * TW <= 2 * Sh::SD_FLOATS, "the window fits the dB/dC scratch");
-    float *const wIn = sdB;                // [2][CH][TWP]: u, Delta_raw
-    float *const wB = sdB + 2 * CH * TWP;  // [TW][NP]
-    float ft[FT], fb[FB];
-    auto load_window = [&](long long t0) {
+    // Sums over the CTA's 32 channels, for every (step, state) of the chunk, of w[c][t] X[c][t][n]:
+    // X = sH (h for dC, dh for dB), w = dy g (dC) or Delta u (dB); into sO[t][WHICH][n].  Thread: step t,
+    // state quad q of state-lane ls, and the channels of one parity (c = 2j + half), which keeps the 8
+    // lanes of a quarter-warp on distinct banks; the parities meet in one shuffle.
+    const int ls = lane & 3, half = (lane >> 2) & 1, qt = (lane >> 3) + 4 * warp;
+    const int sq = qt % NQ, st = qt / NQ;
+    const int kx = (st / G) & 3;  // the swizzle of step st, in channel pairs
+    const float4 *const hcol = sH + (st * NQ + sq) * NTHR + ls + 4 * half;
+    const float *wcol[4];  // row st of sR at channels 2 (jj ^ kx) + half, jj = 0..3 (then + 8 jj' float4)
 #pragma unroll
-        for (int r = 0; r < FT; ++r) {
-            const int q = tid + r * NTHR;
-            const int tens = q / (CH * TW), cc = (q / TW) % CH, i = q % TW;
-            const long long dch = (long long)blockIdx.x * CH + cc;
-            ft[r] = (t0 + i < L && dch < a.Dch) ? IO::load(tens ? a.delta : a.u, (b * a.Dch + dch) * L + t0 + i) : 0.f;
+    for (int jj = 0; jj < 4; ++jj) wcol[jj] = reinterpret_cast<const float *>(sR + st * CH + 2 * (jj ^ kx) + half);
+    auto channel_sums = [&](auto which_tag) {
+        constexpr int WHICH = decltype(which_tag)::value;  // 0: dB (w = Delta u), 1: dC (w = dy g)
+        float2 acc0 = f2(0.f, 0.f), acc1 = f2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < CH / 2; ++j) {
+            // channel 2j + half: its states at hcol[8 j], its weight in swizzled column 2 (j ^ kx) + half
+            const float4 x = hcol[8 * j];
+            const float w = wcol[j & 3][32 * (j >> 2) + 1 + WHICH];
+            acc0 = __ffma2_rn(f2(w, w), f2(x.x, x.y), acc0);
+            acc1 = __ffma2_rn(f2(w, w), f2(x.z, x.w), acc1);
         }
+        acc0.x += __shfl_xor_sync(0xffffffffu, acc0.x, 4);
+        acc0.y += __shfl_xor_sync(0xffffffffu, acc0.y, 4);
+        acc1.x += __shfl_xor_sync(0xffffffffu, acc1.x, 4);
+        acc1.y += __shfl_xor_sync(0xffffffffu, acc1.y, 4);
+        if (half == 0)
+            *reinterpret_cast<float4 *>(sO + (st * 2 + WHICH) * NP + ls * NS + 4 * sq) =
+                make_float4(acc0.x, acc0.y, acc1.x, acc1.y);
+    };
+    // dB, dC of the chunk at t0 (in sO): this thread's (B or C row, 4 steps), one vector atomic add
+    auto flush_sums = [&](long long t0) {
+        float v[4];
 #pragma unroll
-        for (int r = 0; r < FB; ++r) {
-            const int q = tid + r * NTHR;
-            const int n = q / TW, i = q % TW;
-            fb[r] = (t0 + i < L && n < N) ? IO::load(a.Bm, bc0 + (long long)n * L + t0 + i) : 0.f;
+        for (int e = 0; e < 4; ++e) v[e] = sO[((4 * rg + e) * 2 + rwhich) * NP + rn];
+        const int nv = row_valid(t0);
+        float *const dst = (rwhich ? a.dC : a.dB) + bcrow + t0 + 4 * rg;
+        if (vec && nv == 4) {
+            red_add_v4(dst, v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (e < nv) atomicAdd(dst + e, v[e]);
         }
     };
-    auto store_window = [&]() {
+
+    Pack<T, G> pu, pr, pz, pdy;  // this lane's steps of u, Delta_raw, z, dy (one chunk ahead)
+    Pack<T, 4> pbc;              // this thread's 4 steps of its B or C row (one chunk ahead)
+
+    // ---- forward sweep over chunks 0 .. K-2: the state before each chunk k >= 1 goes to the checkpoints
+    float2 h2[NH];
 #pragma unroll
-        for (int r = 0; r < FT; ++r) {
-            const int q = tid + r * NTHR;
-            wIn[(q / TW) * TWP + q % TW] = ft[r];
+    for (int jp = 0; jp < NH; ++jp) h2[jp] = f2(0.f, 0.f);
+    if (K > 1) {
+        pu.load(a.u, row + s * G, lane_valid(0), vec);
+        pr.load(a.delta, row + s * G, lane_valid(0), vec);
+        if (rwhich == 0) pbc.load(a.Bm, bcrow + 4 * rg, row_valid(0), vec);
+    }
+    for (int k = 0; k + 1 < K; ++k) {
+        const long long t0 = (long long)k * TC;
+        __syncthreads();  // the previous chunk's readers are done
+#pragma unroll
+        for (int e = 0; e < G; ++e) {
+            const int i = s * G + e;
+            const bool in = e < lane_valid(t0);
+            const float dl = in ? softplus_of(pr.get(e) + bias) : 0.f;
+            *reinterpret_cast<float2 *>(sR + sw(i, c)) = f2(dl, dl * pu.get(e));
+        }
+        if (rwhich == 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) sBC[(4 * rg + e) * 2 * NP + rn] = pbc.get(e);
+        }
+        __syncthreads();
+        if (k + 2 < K) {  // the next chunk's inputs, in flight during this one
+            pu.load(a.u, row + t0 + TC + s * G, lane_valid(t0 + TC), vec);
+            pr.load(a.delta, row + t0 + TC + s * G, lane_valid(t0 + TC), vec);
+            if (rwhich == 0) pbc.load(a.Bm, bcrow + t0 + TC + 4 * rg, row_valid(t0 + TC), vec);
+        }
+        if (k > 0 && valid) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+                *reinterpret_cast<float4 *>(ck + (long long)k * NP + 4 * q) =
+                    make_float4(h2[2 * q].x, h2[2 * q].y, h2[2 * q + 1].x, h2[2 * q + 1].y);
         }
 #pragma unroll
-        for (int r = 0; r < FB; ++r) {
-            const int q = tid + r * NTHR;
-            wB[(q % TW) * NP + q / TW] = fb[r];
-        }
-    };
-    const long long nwin = (L + TW - 1) / TW;
-    load_window(0);
-    for (long long w = 0; w < nwin; ++w) {
-        __syncthreads();
-        store_window();
-        __syncthreads();
-        if (w + 1 < nwin) load_window((w + 1) * TW);  // in flight during this window
+        for (int i = 0; i < TC; ++i) {
+            const float2 r = *reinterpret_cast<const float2 *>(sR + sw(i, c));
+            const float2 dl2 = f2(r.x, r.x), du2 = f2(r.y, r.y);
 #pragma unroll
-        for (int i = 0; i < TW; ++i) {
-            const long long t = w * TW + i;
-            if (t < L) {  // uniform
-                if (i % TC == 0) {
+            for (int q = 0; q < NQ; ++q) {
+                const float4 bq = *reinterpret_cast<const float4 *>(sBC + i * 2 * NP + s * NS + 4 * q);
+                const float2 bb[2] = {f2(bq.x, bq.y), f2(bq.z, bq.w)};
 #pragma unroll
-                    for (int j = 0; j < NS; ++j)
-                        if (live[j]) ck[(t / TC) * N + j] = (j & 1) ? h2[j / 2].y : h2[j / 2].x;
-                }
-                const float dl = softplus_of(wIn[(CH + c) * TWP + i] + bias);
-                const float du = dl * wIn[c * TWP + i];
-                const float2 dl2 = f2(dl, dl), du2 = f2(du, du);
-                const float2 *wb = reinterpret_cast<const float2 *>(wB + i * NP + s * NS);
-#pragma unroll
-                for (int jp = 0; jp < NH; ++jp) {
-                    const float2 x = __fmul2_rn(dl2, A2p[jp]);
-                    h2[jp] = __ffma2_rn(f2(ex2_approx(x.x), ex2_approx(x.y)), h2[jp], __fmul2_rn(du2, wb[jp]));
+                for (int h = 0; h < 2; ++h) {
+                    const int jp = 2 * q + h;
+                    const float2 x = __fmul2_rn(dl2, A2[jp]);
+                    h2[jp] = __ffma2_rn(f2(ex2_approx(x.x), ex2_approx(x.y)), h2[jp], __fmul2_rn(du2, bb[h]));
                 }
             }
         }
     }
+    // h2 now holds the state before the last chunk
 
     // ---- reverse sweep, chunk by chunk
     float2 dh2[NH], dA2[NH];
 #pragma unroll
     for (int jp = 0; jp < NH; ++jp) dh2[jp] = dA2[jp] = f2(0.f, 0.f);
     float dDacc = 0.f, dbacc = 0.f;
-    float hnext[NS];  // checkpoint of the next chunk to process, loaded one chunk ahead
-    load_chunk((K - 1) * TC, chunk_len(K - 1), 4);
+    {
+        const long long t0 = (long long)(K - 1) * TC;
+        pu.load(a.u, row + t0 + s * G, lane_valid(t0), vec);
+        pr.load(a.delta, row + t0 + s * G, lane_valid(t0), vec);
+        if (HAS_Z) pz.load(a.z, row + t0 + s * G, lane_valid(t0), vec);
+        pdy.load(a.dy, row + t0 + s * G, lane_valid(t0), vec);
+        pbc.load(rwhich ? a.Cm : a.Bm, bcrow + t0 + 4 * rg, row_valid(t0), vec);
+    }
+    float4 hnext[NQ];  // the checkpoint of the next chunk to process, loaded one chunk ahead
 #pragma unroll
-    for (int j = 0; j < NS; ++j) hnext[j] = live[j] ? ck[(K - 1) * N + j] : 0.f;
-    for (long long k = K - 1; k >= 0; --k) {
-        const long long t0 = k * TC;
-        const int nt = chunk_len(k);
-        __syncthreads();
-        store_chunk();
-        __syncthreads();
-        float hstart[NS], dlr[TC];
+    for (int q = 0; q < NQ; ++q)
+        hnext[q] = make_float4(h2[2 * q].x, h2[2 * q].y, h2[2 * q + 1].x, h2[2 * q + 1].y);
+    for (int k = K - 1; k >= 0; --k) {
+        const long long t0 = (long long)k * TC;
+        __syncthreads();  // the previous chunk's readers are done
+        if (k + 1 < K) flush_sums(t0 + TC);
+        // per (channel, step) values of this chunk, this lane's G steps
 #pragma unroll
-        for (int j = 0; j < NS; ++j) hstart[j] = hnext[j];
-#pragma unroll
-        for (int jp = 0; jp < NH; ++jp) h2[jp] = f2(hnext[2 * jp], hnext[2 * jp + 1]);
-        if (k > 0) {  // in flight during this chunk
-            load_chunk((k - 1) * TC, TC, 4);
-#pragma unroll
-            for (int j = 0; j < NS; ++j) hnext[j] = live[j] ? ck[(k - 1) * N + j] : 0.f;
-        }
-        // the chunk body, without per-step length tests for whole chunks (all but possibly the last)
-        auto sweep = [&](auto full_tag) {
-            constexpr bool FULLC = decltype(full_tag)::value;
-#pragma unroll
-            for (int i = 0; i < TC; ++i) {  // recompute the chunk's states (private to this lane)
-                dlr[i] = 0.f;
-                if (FULLC || i < nt) {
-                    const float dl = softplus_of(in_r[i] + bias);
-                    dlr[i] = dl;
-                    const float du = dl * in_u[i];
-                    const float2 dl2 = f2(dl, dl), du2 = f2(du, du);
-                    const float2 *bp = reinterpret_cast<const float2 *>(sBC + i * NP + s * NS);
-#pragma unroll
-                    for (int jp = 0; jp < NH; ++jp) {
-                        const float2 x = __fmul2_rn(dl2, A2p[jp]);
-                        h2[jp] = __ffma2_rn(f2(ex2_approx(x.x), ex2_approx(x.y)), h2[jp], __fmul2_rn(du2, bp[jp]));
-                        sH[(i * NS + 2 * jp) * NTHR + tid] = h2[jp].x;
-                        sH[(i * NS + 2 * jp + 1) * NTHR + tid] = h2[jp].y;
-                    }
+        for (int e = 0; e < G; ++e) {
+            const int i = s * G + e;
+            float dl = 0.f, uu = 0.f, dyh = 0.f, sig = 0.f, gz = 0.f;
+            if (e < lane_valid(t0)) {
+                const float raw = pr.get(e) + bias;
+                uu = pu.get(e);
+                dl = softplus_of(raw);
+                sig = a.softplus ? rcp_approx(1.f + ex2_approx(-raw * kLog2e)) : 1.f;
+                const float dy = pdy.get(e);
+                if (HAS_Z) {
+                    const float zt = pz.get(e);
+                    const float sz = rcp_approx(1.f + ex2_approx(-zt * kLog2e));
+                    dyh = dy * zt * sz;
+                    gz = dy * sz * fmaf(zt, 1.f - sz, 1.f);
+                } else {
+                    dyh = dy;
                 }
             }
-            float hcur[NS];  // h_t of the step being swept (h_{t-1} of the step after it)
+            sR[sw(i, c)] = make_float4(dl, dl * uu, dyh, uu);
+            sE[sw(i, c)] = make_float4(sig, gz, 0.f, 0.f);
+        }
 #pragma unroll
-            for (int j = 0; j < NS; ++j) hcur[j] = sH[((FULLC ? TC - 1 : nt - 1) * NS + j) * NTHR + tid];
+        for (int e = 0; e < 4; ++e) sBC[((4 * rg + e) * 2 + rwhich) * NP + rn] = pbc.get(e);
+        __syncthreads();
+        float4 hstart[NQ];
 #pragma unroll
-            for (int i = TC - 1; i >= 0; --i) {
-                if (!FULLC && i >= nt) continue;
-                const float dl = dlr[i];
-                const float raw = in_r[i] + bias;
-                const float uu = in_u[i], dyt = in_dy[i];
-                float Bt[NS], Ct[NS], hprev[NS];
-                load_vec<NS>(Bt, sBC + i * NP + s * NS);
-                load_vec<NS>(Ct, sBC + (TC + i) * NP + s * NS);
+        for (int q = 0; q < NQ; ++q) hstart[q] = hnext[q];
+        if (k > 0) {  // the next chunk's inputs and checkpoint, in flight during this one
+            const long long tn = t0 - TC;
+            pu.load(a.u, row + tn + s * G, lane_valid(tn), vec);
+            pr.load(a.delta, row + tn + s * G, lane_valid(tn), vec);
+            if (HAS_Z) pz.load(a.z, row + tn + s * G, lane_valid(tn), vec);
+            pdy.load(a.dy, row + tn + s * G, lane_valid(tn), vec);
+            pbc.load(rwhich ? a.Cm : a.Bm, bcrow + tn + 4 * rg, row_valid(tn), vec);
 #pragma unroll
-                for (int j = 0; j < NS; ++j) hprev[j] = i > 0 ? sH[((i - 1) * NS + j) * NTHR + tid] : hstart[j];
-                float g = 1.f, dzt = 0.f;
-                if (has_z) {  // yhat = C . h_t + D u, the C . h part summed over the 4 lanes
-                    float2 ch2 = f2(0.f, 0.f);
+            for (int q = 0; q < NQ; ++q)
+                hnext[q] = (k > 1 && valid) ? *reinterpret_cast<const float4 *>(ck + (long long)(k - 1) * NP + 4 * q)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // recompute the chunk's states h_t into sH
 #pragma unroll
-                    for (int jp = 0; jp < NH; ++jp)
-                        ch2 = __ffma2_rn(f2(Ct[2 * jp], Ct[2 * jp + 1]), f2(hcur[2 * jp], hcur[2 * jp + 1]), ch2);
-                    float ch = ch2.x + ch2.y;
-                    ch += __shfl_xor_sync(0xffffffffu, ch, 1);
-                    ch += __shfl_xor_sync(0xffffffffu, ch, 2);
-                    const float zt = in_z[i];
-                    const float sg = rcp_approx(1.f + ex2_approx(-zt * kLog2e));
-                    g = zt * sg;
-                    dzt = dyt * fmaf(Dd, uu, ch) * sg * fmaf(zt, 1.f - sg, 1.f);
+        for (int q = 0; q < NQ; ++q) {
+            h2[2 * q] = f2(hstart[q].x, hstart[q].y);
+            h2[2 * q + 1] = f2(hstart[q].z, hstart[q].w);
+        }
+#pragma unroll
+        for (int i = 0; i < TC; ++i) {
+            const float2 r = *reinterpret_cast<const float2 *>(sR + sw(i, c));
+            const float2 dl2 = f2(r.x, r.x), du2 = f2(r.y, r.y);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float4 bq = *reinterpret_cast<const float4 *>(sBC + i * 2 * NP + s * NS + 4 * q);
+                const float2 bb[2] = {f2(bq.x, bq.y), f2(bq.z, bq.w)};
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int jp = 2 * q + h;
+                    const float2 x = __fmul2_rn(dl2, A2[jp]);
+                    h2[jp] = __ffma2_rn(f2(ex2_approx(x.x), ex2_approx(x.y)), h2[jp], __fmul2_rn(du2, bb[h]));
                 }
-                const float dyh = dyt * g;
-                // with dh_n after the C term and w_n = dh_n a_n h_{t-1,n}:  du gets Delta q, dDelta gets u q +
-                // sum_n A_n w_n (q = sum_n dh_n B_n), dA_n gets Delta w_n
-                const float dluu = dl * uu;
-                const float2 dl2 = f2(dl, dl), dluu2 = f2(dluu, dluu), dyh2 = f2(dyh, dyh);
-                float2 q2 = f2(0.f, 0.f), wa2 = f2(0.f, 0.f);
+                sH[(i * NQ + q) * NTHR + tid] = make_float4(h2[2 * q].x, h2[2 * q].y, h2[2 * q + 1].x, h2[2 * q + 1].y);
+            }
+        }
+        __syncthreads();
+        channel_sums(std::integral_constant<int, 1>{});  // dC = sum_c dy g h
+        __syncthreads();  // sH is rewritten with dh below
+        // reverse sweep over the chunk; dh_t goes to sH in place of h_t once h_t has been used
+        float2 ht[NH];  // h_t of the step being swept
 #pragma unroll
-                for (int jp = 0; jp < NH; ++jp) {
-                    const int j = 2 * jp;
-                    const float2 ht = f2(hcur[j], hcur[j + 1]), hp = f2(hprev[j], hprev[j + 1]);
-                    hcur[j] = hp.x;
-                    hcur[j + 1] = hp.y;
-                    const float2 tc = __fmul2_rn(dyh2, ht);
-                    sdC[(i * NP + s * NS + j) * Sh::CHP + dcol] = tc.x;
-                    sdC[(i * NP + s * NS + j + 1) * Sh::CHP + dcol] = tc.y;
-                    const float2 dhj = __ffma2_rn(dyh2, f2(Ct[j], Ct[j + 1]), dh2[jp]);
-                    const float2 x = __fmul2_rn(dl2, A2p[jp]);
+        for (int jp = 0; jp < NH; ++jp) ht[jp] = h2[jp];
+#pragma unroll
+        for (int i = TC - 1; i >= 0; --i) {
+            const float4 r = sR[sw(i, c)];  // Delta, Delta u, dy g, u
+            const float2 dl2 = f2(r.x, r.x), dyh2 = f2(r.z, r.z);
+            float2 q2 = f2(0.f, 0.f), wa2 = f2(0.f, 0.f), ch2 = f2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float4 bq = *reinterpret_cast<const float4 *>(sBC + i * 2 * NP + s * NS + 4 * q);
+                const float4 cq = *reinterpret_cast<const float4 *>(sBC + (i * 2 + 1) * NP + s * NS + 4 * q);
+                const float4 hv = i > 0 ? sH[((i - 1) * NQ + q) * NTHR + tid] : hstart[q];  // h_{t-1}
+                const float2 bb[2] = {f2(bq.x, bq.y), f2(bq.z, bq.w)}, cc2[2] = {f2(cq.x, cq.y), f2(cq.z, cq.w)};
+                const float2 hp[2] = {f2(hv.x, hv.y), f2(hv.z, hv.w)};
+                float2 dht[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int jp = 2 * q + h;
+                    dht[h] = __ffma2_rn(dyh2, cc2[h], dh2[jp]);
+                    q2 = __ffma2_rn(dht[h], bb[h], q2);
+                    if (HAS_Z) ch2 = __ffma2_rn(cc2[h], ht[jp], ch2);
+                    const float2 x = __fmul2_rn(dl2, A2[jp]);
                     const float2 e = f2(ex2_approx(x.x), ex2_approx(x.y));
-                    const float2 tb = __fmul2_rn(dhj, dluu2);
-                    sdB[(i * NP + s * NS + j) * Sh::CHP + dcol] = tb.x;
-                    sdB[(i * NP + s * NS + j + 1) * Sh::CHP + dcol] = tb.y;
-                    q2 = __ffma2_rn(dhj, f2(Bt[j], Bt[j + 1]), q2);  // (Bt, Ct from the chunk's B/C rows)
-                    const float2 w = __fmul2_rn(dhj, __fmul2_rn(e, hp));
+                    const float2 w = __fmul2_rn(dht[h], __fmul2_rn(e, hp[h]));
                     dA2[jp] = __ffma2_rn(dl2, w, dA2[jp]);
-                    wa2 = __ffma2_rn(Anp[jp], w, wa2);
-                    dh2[jp] = __fmul2_rn(dhj, e);
+                    wa2 = __ffma2_rn(A2[jp], w, wa2);
+                    dh2[jp] = __fmul2_rn(dht[h], e);
+                    ht[jp] = hp[h];
                 }
-                const float q = q2.x + q2.y, wa = wa2.x + wa2.y;
-                float dup = dl * q, ddt = fmaf(uu, q, wa);
-                dup += __shfl_xor_sync(0xffffffffu, dup, 1);
-                dup += __shfl_xor_sync(0xffffffffu, dup, 2);
-                ddt += __shfl_xor_sync(0xffffffffu, ddt, 1);
-                ddt += __shfl_xor_sync(0xffffffffu, ddt, 2);
-                if (s == 0) {
-                    const float draw = a.softplus ? ddt * rcp_approx(1.f + ex2_approx(-raw * kLog2e)) : ddt;
-                    sOut[c * TCP + i] = fmaf(Dd, dyh, dup);
-                    sOut[(CH + c) * TCP + i] = draw;
-                    sOut[(2 * CH + c) * TCP + i] = dzt;
-                    if (valid) {
-                        dDacc = fmaf(dyh, uu, dDacc);
-                        dbacc += draw;
-                    }
-                }
+                sH[(i * NQ + q) * NTHR + tid] = make_float4(dht[0].x, dht[0].y, dht[1].x, dht[1].y);
             }
-        };
-        if (nt == TC)
-            sweep(std::true_type{});
-        else
-            sweep(std::false_type{});
-        __syncthreads();
-        // this chunk's du, ddelta, dz rows, and dB, dC summed over the CTA's channels (one atomic add
-        // per CTA and element)
-        for (int q = tid; q < (has_z ? 3 : 2) * CH * TC; q += NTHR) {
-            const int tens = q / (CH * TC), cc = (q / TC) % CH, i = q % TC;
-            const long long dch = (long long)blockIdx.x * CH + cc;
-            if (i < nt && dch < a.Dch)
-                IO::store(tens == 0 ? a.du : tens == 1 ? a.ddelta : a.dz, (b * a.Dch + dch) * L + t0 + i,
-                          sOut[(q / TC) * TCP + i]);
+            // sums over the channel's 4 lanes: lane s keeps the total of entry 2 (s & 1) + (s >> 1)
+            float *const qrow = reinterpret_cast<float *>(sQ + sw(i, c));
+            if (HAS_Z) {
+                float v[4] = {q2.x + q2.y, wa2.x + wa2.y, ch2.x + ch2.y, 0.f};
+                transpose_level<2, 1>(v, lane);
+                transpose_level<1, 2>(v, lane);
+                qrow[2 * (s & 1) + (s >> 1)] = v[0];
+            } else {
+                float v[2] = {q2.x + q2.y, wa2.x + wa2.y};
+                transpose_level<1, 1>(v, lane);
+                v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
+                qrow[s & 1] = v[0];
+            }
         }
-        for (int q = tid; q < nt * NP; q += NTHR) {
-            const int i = q / NP, n = q % NP;
-            if (n < N) {
-                const float *pb = sdB + (i * NP + n) * Sh::CHP, *pc = sdC + (i * NP + n) * Sh::CHP;
-                float sb4[4] = {0.f, 0.f, 0.f, 0.f}, sc4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+        __syncthreads();
+        channel_sums(std::integral_constant<int, 0>{});  // dB = sum_c Delta u dh
+        // du, ddelta, dz of this lane's G steps
+        {
+            Pack<T, G> odu, odd, odz;
 #pragma unroll
-                for (int cc = 0; cc < CH; ++cc) {
-                    sb4[cc & 3] += pb[cc];
-                    sc4[cc & 3] += pc[cc];
+            for (int e = 0; e < G; ++e) {
+                const int i = s * G + e;
+                const float4 r = sR[sw(i, c)];
+                const float4 ex = sE[sw(i, c)];
+                const float4 qv = sQ[sw(i, c)];  // q, wa / ln2, C.h
+                const float ddt = fmaf(r.w, qv.x, qv.y * kLn2);
+                const float draw = ddt * ex.x;
+                odu.set(e, fmaf(r.x, qv.x, Dd * r.z));
+                odd.set(e, draw);
+                if (HAS_Z) odz.set(e, ex.y * fmaf(Dd, r.w, qv.z));
+                if (e < lane_valid(t0)) {
+                    dDacc = fmaf(r.z, r.w, dDacc);
+                    dbacc += draw;
                 }
-                const float sb = (sb4[0] + sb4[1]) + (sb4[2] + sb4[3]), sc = (sc4[0] + sc4[1]) + (sc4[2] + sc4[3]);
-                atomicAdd(a.dB + bc0 + (long long)n * L + t0 + i, sb);
-                atomicAdd(a.dC + bc0 + (long long)n * L + t0 + i, sc);
             }
+            const int nv = lane_valid(t0);
+            const long long o = row + t0 + s * G;
+            odu.store(a.du, o, nv, vec);
+            odd.store(a.ddelta, o, nv, vec);
+            if (HAS_Z) odz.store(a.dz, o, nv, vec);
         }
     }
+    __syncthreads();
+    flush_sums(0);
+    // dA, dD, dbias
 #pragma unroll
-    for (int j = 0; j < NS; ++j)
-        if (live[j]) atomicAdd(a.dA + dd * N + (long long)s * NS + j, (j & 1) ? dA2[j / 2].y : dA2[j / 2].x);
+    for (int jp = 0; jp < NH; ++jp) {
+#pragma unroll
+        for (int k2 = 0; k2 < 2; ++k2) {
+            const long long n = (long long)s * NS + 2 * jp + k2;
+            if (valid && n < N) atomicAdd(a.dA + dd * N + n, k2 ? dA2[jp].y : dA2[jp].x);
+        }
+    }
+    dDacc += __shfl_xor_sync(0xffffffffu, dDacc, 1);
+    dDacc += __shfl_xor_sync(0xffffffffu, dDacc, 2);
+    dbacc += __shfl_xor_sync(0xffffffffu, dbacc, 1);
+    dbacc += __shfl_xor_sync(0xffffffffu, dbacc, 2);
     if (valid && s == 0) {
         if (a.dD != nullptr) atomicAdd(a.dD + dd, dDacc);
         if (a.dbias != nullptr) atomicAdd(a.dbias + dd, dbacc);
     }
 }
 
-template <typename T, int NS>
-static cudaError_t launch_bwd_ns(const BwdArgs &a, long long Bsz, long long K, cudaStream_t st) {
-    using Sh = BwdShape<T, NS>;
-    auto kern = scan_bwd_kernel<T, NS>;
-    if (Sh::SMEM_BYTES > 48 * 1024) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM_BYTES);
+template <typename T, int NS, bool HAS_Z>
+static cudaError_t launch_bwd_ns(const BwdArgs &a, long long Bsz, int K, cudaStream_t st) {
+    using Sh = BwdShape<NS>;
+    auto kern = scan_bwd_kernel<T, NS, HAS_Z>;
+    static bool attr_set[kMaxDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Sh::SMEM_BYTES);
         if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < kMaxDevices) attr_set[dev] = true;
     }
     dim3 grid((unsigned)((a.Dch + Sh::CH - 1) / Sh::CH), (unsigned)Bsz, 1);
     kern<<<grid, Sh::NTHR, Sh::SMEM_BYTES, st>>>(a, K);
     return cudaGetLastError();
 }
 
-// steps per checkpoint chunk for N states
-int bwd_chunk_steps(long long N) { return N <= 16 ? 8 : N <= 32 ? 4 : 2; }
+template <typename T, int NS>
+static cudaError_t launch_bwd_z(const BwdArgs &a, long long Bsz, int K, cudaStream_t st) {
+    return a.z != nullptr ? launch_bwd_ns<T, NS, true>(a, Bsz, K, st) : launch_bwd_ns<T, NS, false>(a, Bsz, K, st);
+}
+
+// states per lane, steps per checkpoint chunk and padded state count for N states
+static int bwd_ns(long long N) { return N <= 16 ? 4 : N <= 32 ? 8 : 16; }
+int bwd_chunk_steps(long long N) { return 64 / bwd_ns(N); }
 
 cudaError_t launch_scan_bwd(int dtype, const BwdArgs &a, long long Bsz, cudaStream_t st) {
-    const long long K = (a.L + bwd_chunk_steps(a.N) - 1) / bwd_chunk_steps(a.N);
-    if (dtype == 1) {
-        if (a.N <= 16) return launch_bwd_ns<bf16_t, 4>(a, Bsz, K, st);
-        if (a.N <= 32) return launch_bwd_ns<bf16_t, 8>(a, Bsz, K, st);
-        return launch_bwd_ns<bf16_t, 16>(a, Bsz, K, st);
+    const int K = (int)((a.L + bwd_chunk_steps(a.N) - 1) / bwd_chunk_steps(a.N));
+    switch (bwd_ns(a.N) + (dtype == 1 ? 100 : 0)) {
+        case 104: return launch_bwd_z<bf16_t, 4>(a, Bsz, K, st);
+        case 108: return launch_bwd_z<bf16_t, 8>(a, Bsz, K, st);
+        case 116: return launch_bwd_z<bf16_t, 16>(a, Bsz, K, st);
+        case 4: return launch_bwd_z<float, 4>(a, Bsz, K, st);
+        case 8: return launch_bwd_z<float, 8>(a, Bsz, K, st);
+        default: return launch_bwd_z<float, 16>(a, Bsz, K, st);
     }
-    if (a.N <= 16) return launch_bwd_ns<float, 4>(a, Bsz, K, st);
-    if (a.N <= 32) return launch_bwd_ns<float, 8>(a, Bsz, K, st);
-    return launch_bwd_ns<float, 16>(a, Bsz, K, st);
 }
 
 }  // namespace mamba
@@ -435,13 +534,15 @@ extern "C" int mamba_selective_scan_bwd(const void *u, const void *delta, const 
     if (z != nullptr && dz == nullptr) return MAMBA_ERR_NULL_ARG;
     if (dtype != MAMBA_F32 && dtype != MAMBA_BF16) return MAMBA_ERR_BAD_DTYPE;
     constexpr long long kMax = 1LL << 40;
+    const long long Kc = (L + 3) / 4;  // checkpoint chunks are at least 4 steps
     if (Bsz <= 0 || Dch <= 0 || L <= 0 || N <= 0 || Bsz > 65535 || Dch > kMax || L > kMax ||
-        Bsz * Dch > kMax / L || Bsz * N > kMax / L)
+        Bsz * Dch > kMax / L || Bsz * N > kMax / L || Bsz * Dch > kMax / (Kc * 64) || Kc > (1LL << 30))
         return MAMBA_ERR_BAD_SHAPE;
     if (N > 64) return MAMBA_ERR_UNSUPPORTED_N;
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const long long K = (L + bwd_chunk_steps(N) - 1) / bwd_chunk_steps(N);
-    const size_t ck_bytes = (size_t)(Bsz * Dch) * (size_t)K * (size_t)N * sizeof(float);
+    const long long NP = 4LL * bwd_ns(N);
+    const size_t ck_bytes = (size_t)(Bsz * Dch) * (size_t)K * (size_t)NP * sizeof(float);
     void *ck = nullptr;
     const char *inject = std::getenv("MAMBA_FAULT_INJECT");  // host-side test hook, as in the forward scan
     if (inject != nullptr && std::strcmp(inject, "alloc") == 0) return MAMBA_ERR_ALLOC;
@@ -481,6 +582,11 @@ extern "C" int mamba_selective_scan_bwd(const void *u, const void *delta, const 
         a.L = L;
         a.N = N;
         a.softplus = softplus_flag ? 1 : 0;
+        auto al16 = [](const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+        a.vec = (L % 4 == 0 && al16(u) && al16(delta) && al16(z) && al16(B) && al16(C) && al16(dy) && al16(du) &&
+                 al16(ddelta) && al16(dz) && al16(dB) && al16(dC))
+                    ? 1
+                    : 0;
         if (launch_scan_bwd(dtype, a, Bsz, st) != cudaSuccess) rc = MAMBA_ERR_LAUNCH;
     }
     if (cudaFreeAsync(ck, st) != cudaSuccess) {
