@@ -163,9 +163,11 @@ scan_bwd_kernel(const BwdArgs a, int K) {
     // B/C rows and dB/dC sums: thread -> (which = B or C, state n, 4-step group rg)
     const int rg = tid % (TC / 4), rrow = tid / (TC / 4), rwhich = rrow / NP, rn = rrow % NP;
     const long long bcrow = (b * N + (rn < N ? rn : 0)) * L;
-    // [TC][CH] arrays: the column of channel c at step i is c ^ (2 (i / G mod 4)), so that the 4 lanes
-    // of a channel, which take consecutive groups of G steps, write and read distinct banks
-    auto sw = [&](int i, int cc) { return i * CH + (cc ^ (2 * ((i / G) & 3))); };
+    // [TC][CH] arrays: the column of channel c at step i is c ^ 2 f(i), f(i) = (i / G xor i) mod 4 (i mod 4
+    // for G = 1): the 4 lanes of a channel, which take consecutive groups of G steps, and the 4 steps that
+    // a warp's channel sums read at once fall on distinct banks
+    auto swz = [](int i) { return 2 * (((i / G) ^ (G == 1 ? 0 : i)) & 3); };
+    auto sw = [&](int i, int cc) { return i * CH + (cc ^ swz(i)); };
 
     // per-state constants in pairs of adjacent states (f32x2): A log2 e
     float2 A2[NH];
@@ -200,7 +202,7 @@ scan_bwd_kernel(const BwdArgs a, int K) {
     // lanes of a quarter-warp on distinct banks; the parities meet in one shuffle.
     const int ls = lane & 3, half = (lane >> 2) & 1, qt = (lane >> 3) + 4 * warp;
     const int sq = qt % NQ, st = qt / NQ;
-    const int kx = (st / G) & 3;  // the swizzle of step st, in channel pairs
+    const int kx = swz(st) / 2;  // the swizzle of step st, in channel pairs
     const float4 *const hcol = sH + (st * NQ + sq) * NTHR + ls + 4 * half;
     const float *wcol[4];  // row st of sR at channels 2 (jj ^ kx) + half, jj = 0..3 (then + 8 jj' float4)
 #pragma unroll
@@ -365,6 +367,7 @@ scan_bwd_kernel(const BwdArgs a, int K) {
             h2[2 * q] = f2(hstart[q].x, hstart[q].y);
             h2[2 * q + 1] = f2(hstart[q].z, hstart[q].w);
         }
+        float2 hreg[TC][NH];  // the chunk's states, also kept in registers for the reverse sweep
 #pragma unroll
         for (int i = 0; i < TC; ++i) {
             const float2 r = *reinterpret_cast<const float2 *>(sR + sw(i, c));
@@ -378,6 +381,7 @@ scan_bwd_kernel(const BwdArgs a, int K) {
                     const int jp = 2 * q + h;
                     const float2 x = __fmul2_rn(dl2, A2[jp]);
                     h2[jp] = __ffma2_rn(f2(ex2_approx(x.x), ex2_approx(x.y)), h2[jp], __fmul2_rn(du2, bb[h]));
+                    hreg[i][jp] = h2[jp];
                 }
                 sH[(i * NQ + q) * NTHR + tid] = make_float4(h2[2 * q].x, h2[2 * q].y, h2[2 * q + 1].x, h2[2 * q + 1].y);
             }
@@ -398,7 +402,9 @@ scan_bwd_kernel(const BwdArgs a, int K) {
             for (int q = 0; q < NQ; ++q) {
                 const float4 bq = *reinterpret_cast<const float4 *>(sBC + i * 2 * NP + s * NS + 4 * q);
                 const float4 cq = *reinterpret_cast<const float4 *>(sBC + (i * 2 + 1) * NP + s * NS + 4 * q);
-                const float4 hv = i > 0 ? sH[((i - 1) * NQ + q) * NTHR + tid] : hstart[q];  // h_{t-1}
+                const float4 hv = i > 0 ? make_float4(hreg[i - 1][2 * q].x, hreg[i - 1][2 * q].y, hreg[i - 1][2 * q + 1].x,
+                                                      hreg[i - 1][2 * q + 1].y)
+                                        : hstart[q];  // h_{t-1}
                 const float2 bb[2] = {f2(bq.x, bq.y), f2(bq.z, bq.w)}, cc2[2] = {f2(cq.x, cq.y), f2(cq.z, cq.w)};
                 const float2 hp[2] = {f2(hv.x, hv.y), f2(hv.z, hv.w)};
                 float2 dht[2];
