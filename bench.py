@@ -587,8 +587,13 @@ def scan_result(args, m, torch, x, workload, steps, conv, t_ms, clocks, chunked,
         roof = {"bound": "hbm", "achieved": round(nbytes / t_meas / 1e9, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(t_hbm / t_meas, 4), "traffic": traffic, "kernel": kernel,
                 "peak_source": f"{peaks['source']} copy bandwidth"}
+    scheme = ("two-pass" if (os.environ.get("MAMBA_CHUNKED_SCAN") == "two-pass" or not tm or flag_name != "none"
+                             or conv == "fused") else "decay-truncated")
     if chunked:
-        roof["note"] = "chunked scan: the step is three launches (chunk states, carry, rescan); figures are per step"
+        roof["note"] = (f"chunked scan ({scheme}): the step is three launches "
+                        + ("(every chunk from a zero state with its end state, carry, correction of y)"
+                           if scheme == "decay-truncated" else "(chunk end states, carry, rescan)")
+                        + "; figures are per step")
     if conv == "two-step":
         roof["note"] = (roof.get("note", "") + "; " if "note" in roof else "") + \
             "two launches per step (convolution, then scan); figures are per step"
@@ -596,7 +601,7 @@ def scan_result(args, m, torch, x, workload, steps, conv, t_ms, clocks, chunked,
                 config={"workload": workload, "batch": Bsz, "d_inner": Dch, "d_state": N, "seq_len": L,
                         "io": io, "state": "fp32", "l2": f"inputs rotate over {R} resident copies "
                                                           f"({R * nbytes / 1e6:.0f} MB > L2)",
-                        "path": "chunked" if chunked else "direct",
+                        "path": f"chunked ({scheme})" if chunked else "direct",
                         **({"flags": flag_name} if flag_name != "none" else {}),
                         **({"conv": conv + " (depthwise causal conv1d k=4 + SiLU feeding u)"}
                            if conv != "none" else {})},

@@ -117,17 +117,17 @@ int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A, c
  *               > 0: force the chunked scan with chunks of this many steps
  *                    (rounded up to the kernel's time tile);
  *               < 0: force the direct (single pass) scan.
- *               The chunked scan is the two-pass one (chunk end states from a
- *               zero state, the carry, every chunk again from its entering
- *               state).  With the environment variable
- *               MAMBA_CHUNKED_SCAN=truncated (read on every call) a call
- *               without flags, aligned, 8 < N <= 64, chunk_len a multiple of
- *               32 and no convolution runs the decay-truncated scan instead:
- *               every chunk once from a zero state (y, end state), the carry,
- *               then y += the entering state's contribution, decayed with no
- *               input, up to where it falls below 2^-40 of that state (only
- *               when the decay is monotone: softplus on, every A <= 0).  It is
- *               faster only when every channel's steps are large.
+ *               A call without flags, aligned, 8 < N <= 64 (fp32: N <= 16),
+ *               chunk_len a multiple of 32 and no convolution runs the
+ *               decay-truncated chunked scan: every chunk once from a zero
+ *               state (y, end state), the carry, then y += the entering
+ *               state's contribution, decayed with no input, up to where it
+ *               falls below 2^-40 of that state (only when the decay is
+ *               monotone: softplus on, every A <= 0).  Other calls, and every
+ *               call with the environment variable MAMBA_CHUNKED_SCAN=two-pass
+ *               (read on every call), run the two-pass scan: chunk end states
+ *               from a zero state, the carry, every chunk again from its
+ *               entering state.  Both give the same result up to rounding.
  *   workspace, workspace_bytes
  *               caller-owned device scratch for the chunked scan (256-byte
  *               aligned, at least mamba_scan_workspace_size(...) bytes), or

@@ -91,6 +91,9 @@ int make_plan(long long Bsz, long long Dch, long long L, long long N, int dtype,
             // scan runs K - 1 chunks (end states) and then K chunks (outputs), each pass costing its
             // waves times the chunk length; take the K (narrower chunks only when strictly cheaper)
             // that minimises (cost(K - 1) + cost(K)) * chunk_len, against cost(1) * L for the direct scan.
+            // Narrower chunks must be at least 3 % cheaper: long chunks pay fewer CTA set-ups, and the
+            // correction pass of the decay-truncated scan stops at a fixed number of steps, a smaller
+            // share of a long chunk.
             const int S = N <= 16 ? 4 : N <= 32 ? 8 : 16;
             double best = (double)tm_launch_cost(Bsz, Dch, 1, sms, S, nullptr) * (double)L;
             long long best_cl = L;
@@ -101,7 +104,7 @@ int make_plan(long long Bsz, long long Dch, long long L, long long N, int dtype,
                 if (Kr < 2) continue;
                 const double t = (double)(tm_launch_cost(Bsz, Dch, (int)(Kr - 1), sms, S, nullptr) +
                                           tm_launch_cost(Bsz, Dch, (int)Kr, sms, S, nullptr)) * (double)c;
-                if (t < best * (1.0 - 1e-9)) {
+                if (t < best * (best_cl >= L ? 1.0 - 1e-9 : 0.97)) {
                     best = t;
                     best_cl = c;
                 }

@@ -54,8 +54,8 @@ cudaError_t launch_carry(const float *A, const float *h0, float *ws_h, const flo
 // Whether the decay-truncated chunked scan (tensor-memory kernel) serves these sizes and flags.
 bool tm_chunked_for(int dtype, long long N, int flags, bool vec, bool conv);
 
-// The chunked scan after its workspace is in hand: the decay-truncated scan where it is requested
-// (MAMBA_CHUNKED_SCAN=truncated) and tm_chunked_for holds, else the two-pass scan (chunk end states, carry, seeded rescan).  a.chunk_len and a.nchunks
+// The chunked scan after its workspace is in hand: the decay-truncated scan where tm_chunked_for holds
+// (unless MAMBA_CHUNKED_SCAN=two-pass), else the two-pass scan (chunk end states, carry, seeded rescan).  a.chunk_len and a.nchunks
 // set; ws_h [Bsz][K][Dch][N] and ws_sdt [Bsz][K][Dch]; h0 may be null.
 cudaError_t run_chunked(int dtype, bool vec, ScanArgs a, long long Bsz, float *ws_h, float *ws_sdt,
                         const float *h0, cudaStream_t st);

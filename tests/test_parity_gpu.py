@@ -344,13 +344,18 @@ def test_flags_tensor_memory_path(case, io, N, L):
 
 @pytest.mark.parametrize("regime", ["fast_decay", "slow_decay", "no_softplus", "growing_state"])
 @pytest.mark.parametrize("io", ["bf16", "f32"])
-def test_chunked_scan_correction_regimes(regime, io, monkeypatch):
-    """The decay-truncated chunked scan (MAMBA_CHUNKED_SCAN=truncated) corrects each chunk's y for its
-    entering state and stops where that contribution has decayed below fp32 resolution: a stop after a
-    few tiles (dt near 1), no stop within a 1024-step chunk (dt near 1e-3, the smallest step of the
-    workloads), and the cases where the decay is not guaranteed monotone (softplus off; a positive A)
-    and the correction must run to the end of every chunk.  With and without h0."""
-    monkeypatch.setenv("MAMBA_CHUNKED_SCAN", "truncated")
+@pytest.mark.parametrize("scheme", ["truncated", "two-pass"])
+def test_chunked_scan_correction_regimes(regime, io, scheme, monkeypatch):
+    """The decay-truncated chunked scan (the default) corrects each chunk's y for its entering state and
+    stops where that contribution has decayed below fp32 resolution: a stop after a few tiles (dt near
+    1), no stop within a 1024-step chunk (dt near 1e-3, the smallest step of the workloads), and the
+    cases where the decay is not guaranteed monotone (softplus off; a positive A) and the correction must
+    run to the end of every chunk.  The two-pass scan (MAMBA_CHUNKED_SCAN=two-pass) on the same inputs.
+    With and without h0."""
+    if scheme == "two-pass":
+        monkeypatch.setenv("MAMBA_CHUNKED_SCAN", "two-pass")
+    else:
+        monkeypatch.delenv("MAMBA_CHUNKED_SCAN", raising=False)
     x = inputs.make_scan_inputs(1, 40, 16, 6144, io=io, seed=120)
     softplus = regime != "no_softplus"
     if regime == "fast_decay":
