@@ -122,8 +122,10 @@ int mamba_selective_scan_fwd(const void *u, const void *delta, const float *A, c
  *               decay-truncated chunked scan: every chunk once from a zero
  *               state (y, end state), the carry, then y += the entering
  *               state's contribution, decayed with no input, up to where it
- *               falls below 2^-30 of that state (only when the decay is
- *               monotone: softplus on, every A <= 0).  Other calls, and every
+ *               falls below 2^-16 (bf16 storage) or 2^-30 (fp32 storage) of
+ *               that state, at least 2^7 below the rounding of the stored y
+ *               (only when the decay is monotone: softplus on, every
+ *               A <= 0).  Other calls, and every
  *               call with the environment variable MAMBA_CHUNKED_SCAN=two-pass
  *               (read on every call), run the two-pass scan: chunk end states
  *               from a zero state, the carry, every chunk again from its

@@ -467,7 +467,7 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
     if constexpr (CORR) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            thr[j] = fabsf(hh[j].y) * 0x1p-30f;
+            thr[j] = fabsf(hh[j].y) * (FAST ? 0x1p-16f : 0x1p-30f);
             monotone = monotone && A2d[j].x <= 0.f;
         }
     }
@@ -599,10 +599,11 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                 __syncwarp();  // partials of sub-tile i and Delta of sub-tile i+1 visible to the channel's lanes
             }
             if constexpr (CORR) {
-                // Once every state of the warp has decayed below 2^-30 of the state it entered the chunk
-                // with, it stays there (softplus Delta > 0 and A <= 0: each step multiplies it by
-                // exp(Delta A) <= 1), and what it would still add to y is 64 times below the fp32
-                // rounding of the entering state's contribution: record the super-tile, once.
+                // Once every state of the warp has decayed below 2^-16 (bf16 y) or 2^-30 (fp32 y) of the
+                // state it entered the chunk with, it stays there (softplus Delta > 0 and A <= 0: each step
+                // multiplies it by exp(Delta A) <= 1), and what it would still add to y is 2^7 (bf16: 2^-16
+                // against the 2^-9 rounding of the stored y) or 2^6 (fp32) times below the rounding of the
+                // entering state's contribution: record the super-tile, once.
                 bool small = monotone;
 #pragma unroll
                 for (int j = 0; j < 4; ++j) small = small && fabsf(hh[j].y) <= thr[j];
