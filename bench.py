@@ -559,6 +559,26 @@ def scan_e2e(args, torch, base, sets, ys, hs, run, conv, tdt, Bsz, Dch, N):
     return e2e_ms, h2d, d2h
 
 
+def lean_warps(Bsz, Dch, S, sms):
+    """The compute warps of the lean tensor-memory kernel for a plain direct bf16 scan, 0 for the regular
+    form: the library's rule (csrc/scan_tm.cu, choose_lean_warps), restated to name the kernel that ran."""
+    env = os.environ.get("MAMBA_TM_LEAN")
+    if env == "0":
+        return 0
+
+    def waves(w):
+        cw = 32 * w // S
+        return -(-(Bsz * (-(-Dch // cw))) // sms)
+
+    costs = [(waves(w) * ((w + 1 + 3) // 4), w) for w in range(8, 12)]
+    regular = min(costs)[1]                   # narrowest width of least cost, as tm_launch_cost
+    best, best_waves = 0, (1 << 62) if env == "1" else waves(regular)
+    for w in range(12, 19):
+        if waves(w) < best_waves:
+            best, best_waves = w, waves(w)
+    return best
+
+
 def scan_result(args, m, torch, x, workload, steps, conv, t_ms, clocks, chunked, nbytes, R, e2e_ms, h2d, d2h,
                 mufu_per_clk, sms, flag_name="none"):
     Bsz, Dch, L, N = x.shape
@@ -571,7 +591,11 @@ def scan_result(args, m, torch, x, workload, steps, conv, t_ms, clocks, chunked,
     t_mufu = exps / mufu_peak
     t_meas = t_ms * 1e-3
     tm = 8 < N <= 64 and (io == "bf16" or N <= 16) and os.environ.get("MAMBA_SCAN_KERNEL") != "smem"
-    kernel = (f"scan_tm_kernel<{io},full,z,S{4 if N <= 16 else 8 if N <= 32 else 16}"
+    S = 4 if N <= 16 else 8 if N <= 32 else 16
+    lean = tm and io == "bf16" and conv == "none" and flag_name == "none" and not chunked and \
+        lean_warps(Bsz, Dch, S, sms) > 0
+    kernel = (f"scan_tm_lean_kernel<{io},full,z,S{S},W{lean_warps(Bsz, Dch, S, sms)}>" if lean else
+              f"scan_tm_kernel<{io},full,z,S{S}"
               f"{',conv' if conv == 'fused' else ''}{',flags' if flag_name != 'none' else ''}>" if tm
               else f"scan_kernel<{io},NP{1 << max(2, (N - 1).bit_length())},full>")
     traffic = traffic_record(workload)

@@ -95,6 +95,33 @@ int choose_warps(long long Bsz, long long Dch, int grid_chunks, int sms, int S) 
     return w;
 }
 
+long long waves_of(long long Bsz, long long Dch, int sms, int S, int w) {
+    const long long cw = 32LL * w / S;
+    const long long ctas = Bsz * ((Dch + cw - 1) / cw);
+    return sms > 0 ? (ctas + sms - 1) / sms : 1;
+}
+
+// The lean form (12..18 compute warps, fewer registers per thread) of a direct scan: the narrowest
+// width with the fewest waves, taken when that is fewer waves than the regular width needs (its
+// channels then run with more warps per SM sub-partition).  MAMBA_TM_LEAN=0 / 1 (read on every call)
+// never / always takes it.  Returns 0 for the regular form.
+int choose_lean_warps(long long Bsz, long long Dch, int sms, int S, int regular_warps) {
+    using Sh = TmShape<bf16_t, MODE_FULL, 4, false, true>;
+    const char *v = std::getenv("MAMBA_TM_LEAN");
+    if (v != nullptr && v[0] == '0' && v[1] == '\0') return 0;
+    const bool force = v != nullptr && v[0] == '1' && v[1] == '\0';
+    int best = 0;
+    long long best_waves = force ? (1LL << 62) : waves_of(Bsz, Dch, sms, S, regular_warps);
+    for (int w = Sh::MIN_WARPS; w <= Sh::MAX_WARPS; ++w) {
+        const long long wv = waves_of(Bsz, Dch, sms, S, w);
+        if (wv < best_waves) {
+            best_waves = wv;
+            best = w;
+        }
+    }
+    return best;
+}
+
 }  // namespace
 
 // The kernel's pipeline waits are bounded by time (about a second); MAMBA_TEST_WAIT_POLLS=0, a host-side
@@ -122,7 +149,12 @@ cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &args, long long 
     // the convolution-fed variant is built for bf16, N <= 16, with the gate
     const bool conv = a.conv_w != nullptr;
     if (conv && (!bf16 || S != 4 || (mode == MODE_FULL && a.z == nullptr))) return cudaErrorNotSupported;
-    const int warps = choose_warps(Bsz, a.Dch, grid_chunks, device_sms(), S);
+    int warps = choose_warps(Bsz, a.Dch, grid_chunks, device_sms(), S);
+    // the plain direct bf16 scan may take the lean form (more warps per CTA)
+    const int lean_warps = (bf16 && !conv && mode == MODE_FULL && a.flags == 0 && grid_chunks == 1)
+                               ? choose_lean_warps(Bsz, a.Dch, device_sms(), S, warps)
+                               : 0;
+    if (lean_warps > 0) warps = lean_warps;
     const unsigned ch = 32u * (unsigned)warps / (unsigned)S;
     TmMaps maps;
     const bool ok = (conv ? encode_3d(&maps.u, a.u, bf16, a.L, a.Dch, Bsz, ch, false, TmShape<bf16_t, MODE_FULL, 4, true>::XSTEPS)
@@ -143,6 +175,13 @@ cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &args, long long 
                    ? launch_tm_one<bf16_t, MODE_STATES, false, 4, true>(a, maps, warps, Bsz, grid_chunks, st)
                    : launch_tm_one<bf16_t, MODE_FULL, true, 4, true>(a, maps, warps, Bsz, grid_chunks, st);
     if (!bf16) return launch_tm_s<float, 4>(mode, a, maps, warps, Bsz, grid_chunks, st);
+    if (lean_warps > 0) {
+        switch (S) {
+            case 4: return launch_tm_lean<4>(a, maps, warps, Bsz, st);
+            case 8: return launch_tm_lean<8>(a, maps, warps, Bsz, st);
+            default: return launch_tm_lean<16>(a, maps, warps, Bsz, st);
+        }
+    }
     switch (S) {
         case 4: return launch_tm_s<bf16_t, 4>(mode, a, maps, warps, Bsz, grid_chunks, st);
         case 8: return launch_tm_s<bf16_t, 8>(mode, a, maps, warps, Bsz, grid_chunks, st);

@@ -85,10 +85,14 @@ enum { FL_REV = 1, FL_ZOH = 2 };  // flag variants of the kernel (template argum
 // S = lanes per channel (4, 8 or 16: N <= 4 S), each lane owning 4 states.
 // CONV: the first input tile is x with an 8-step halo (40 steps from t0 - 8,
 // unswizzled) from which u = SiLU(causal conv(x)) is formed.
-template <typename T, int MODE, int S_ = 4, bool CONV = false>
+// LEAN: each lane loads one step pair's 16 TMEM columns at a time instead of a
+// sub-tile's 64, which brings the kernel to 96 registers per thread, so a
+// CTA can run 12..18 compute warps (one CTA per SM still): problems whose
+// channels would need two or more waves of 8..11-warp CTAs fit in fewer.
+template <typename T, int MODE, int S_ = 4, bool CONV = false, bool LEAN = false>
 struct TmShape {
     static constexpr int S = S_;
-    static constexpr int MIN_WARPS = 8, MAX_WARPS = 11;  // compute warps of a CTA, 32 / S channels each
+    static constexpr int MIN_WARPS = LEAN ? 12 : 8, MAX_WARPS = LEAN ? 18 : 11;  // compute warps, 32 / S channels each
     static constexpr int MAX_THR = 32 * MAX_WARPS, MAX_CH = MAX_THR / S;
     static constexpr int LAUNCH_THR = MAX_THR + 32;       // + the producer warp
     static constexpr int TT = 32;                  // steps per super-tile
@@ -135,11 +139,11 @@ struct TmShape {
 // (SCAN_FLAG_REVERSE; fsdata.site explainer §7 table, the reverse SSM);
 // FL_ZOH the exact zero-order-hold input weight (freeguideonline tutorial
 // §2.2), forwards or, with SCAN_FLAG_REVERSE, in reverse.
-// blockDim.x = 32 (W + 1): W compute warps (8..11) and one producer warp.
-template <typename T, int MODE, bool HAS_Z, int S_, bool CONV = false, int FLAGS = 0>
-__global__ void __launch_bounds__(TmShape<T, MODE, S_, CONV>::LAUNCH_THR, 1)
-scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
-    using Sh = TmShape<T, MODE, S_, CONV>;
+// blockDim.x = 32 (W + 1): W compute warps (8..11, lean form 12..18) and one producer warp.
+template <typename T, int MODE, bool HAS_Z, int S_, bool CONV, int FLAGS, bool LEAN>
+__device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &maps) {
+    using Sh = TmShape<T, MODE, S_, CONV, LEAN>;
+    static_assert(!LEAN || (MODE == MODE_FULL && !CONV && FLAGS == 0), "the lean form serves the plain direct scan");
     constexpr bool FAST = sizeof(T) == 2;
     constexpr bool HASY = MODE != MODE_STATES;                             // forms y (and reads C)
     constexpr bool ENDS = MODE == MODE_STATES || MODE == MODE_FULL_STATES;  // writes end states, sum of Delta
@@ -538,21 +542,23 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
 #pragma unroll
             for (int q = 0; q < NSUB; ++q) {
                 // MODE_FULL: step pairs 0, 1 in bcu[0] and 2, 3 in bcu[1], 16 columns each;
-                // MODE_STATES: B of the 4 step pairs in bcu[0] (8 columns each), no C
-                uint32_t bcu[2][32];
-                tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64, bcu[0]);
-                if constexpr (HASY) {
-                    tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64 + 32, bcu[1]);
-                    tc::tmem_wait_ld_tied(bcu[0], bcu[1]);
-                } else {
-                    tc::tmem_wait_ld_tied(bcu[0]);
-                }
-
-                // one block: y of sub-tile i-1, Delta etc. of sub-tile i+1, the
-                // recurrence of sub-tile i (i = 4 sup + q, so i & 1 == q & 1)
-                float4 dq[TB / 2];
+                // MODE_STATES: B of the 4 step pairs in bcu[0] (8 columns each), no C.
+                // LEAN: each pair's 16 columns are loaded in the recurrence below.
+                uint32_t bcu[LEAN ? 1 : 2][32];
+                float4 dq[LEAN ? 1 : TB / 2];
+                if constexpr (!LEAN) {
+                    tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64, bcu[0]);
+                    if constexpr (HASY) {
+                        tc::tmem_ld32_nowait(tmem_lane + (sup & 1) * COLS + q * 64 + 32, bcu[1]);
+                        tc::tmem_wait_ld_tied(bcu[0], bcu[1]);
+                    } else {
+                        tc::tmem_wait_ld_tied(bcu[0]);
+                    }
+                    // one block: y of sub-tile i-1, Delta etc. of sub-tile i+1, the
+                    // recurrence of sub-tile i (i = 4 sup + q, so i & 1 == q & 1)
 #pragma unroll
-                for (int p = 0; p < TB / 2; ++p) dq[p] = du_chan[(q & 1) * MAX_CH * 4 + p];
+                    for (int p = 0; p < TB / 2; ++p) dq[p] = du_chan[(q & 1) * MAX_CH * 4 + p];
+                }
                 output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
                 if (q + 1 < NSUB) {
                     side_pair(st_cur, q + 1, r0 + (q + 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
@@ -564,9 +570,22 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
                 float pq[TB];
 #pragma unroll
                 for (int p = 0; p < TB / 2; ++p) {
-                    const float2 dl = f2(dq[p].x, dq[p].y);
-                    const float2 du = f2(dq[p].z, dq[p].w);
-                    const uint32_t *bcp = HASY ? bcu[p >> 1] + 16 * (p & 1) : bcu[0] + 8 * p;
+                    uint32_t bcl[LEAN ? 16 : 1];
+                    float4 dqp;
+                    const uint32_t *bcp;
+                    if constexpr (LEAN) {
+                        // this pair's B and C columns, and its Delta, Delta u (written in the previous
+                        // sub-tile, before the last __syncwarp)
+                        tc::tmem_ld16_nowait(tmem_lane + (sup & 1) * COLS + q * 64 + 16 * p, bcl);
+                        dqp = du_chan[(q & 1) * MAX_CH * 4 + p];
+                        tc::tmem_wait_ld_tied(bcl);
+                        bcp = bcl;
+                    } else {
+                        dqp = dq[p];
+                        bcp = HASY ? bcu[p >> 1] + 16 * (p & 1) : bcu[0] + 8 * p;
+                    }
+                    const float2 dl = f2(dqp.x, dqp.y);
+                    const float2 du = f2(dqp.z, dqp.w);
                     const uint32_t *ccp = bcp + 8;
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
@@ -664,13 +683,32 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
 }
 
 
+// The kernel: blockDim.x = 32 (W + 1), W = 8..11 compute warps and the producer warp.
+template <typename T, int MODE, bool HAS_Z, int S_, bool CONV = false, int FLAGS = 0>
+__global__ void __launch_bounds__(TmShape<T, MODE, S_, CONV>::LAUNCH_THR, 1)
+scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
+    scan_tm_body<T, MODE, HAS_Z, S_, CONV, FLAGS, false>(a, maps);
+}
+
+// The lean form: W = 12..18 compute warps and the producer warp; at most 96 registers per thread.  A
+// CTA's warps are spread over the SM's 4 sub-partitions, each with a quarter of the register file
+// (16 384 registers): 19 warps put 5 warps on a sub-partition, 5 x 32 x 96 = 15 360.
+template <typename T, int MODE, bool HAS_Z, int S_>
+__global__ void __maxnreg__(96) scan_tm_lean_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
+    scan_tm_body<T, MODE, HAS_Z, S_, false, 0, true>(a, maps);
+}
+
 // Launch of one instantiation: grid (ceil(Dch / channels per CTA), Bsz, grid_chunks), W compute warps
 // plus the producer warp, one CTA per SM.
-template <typename T, int MODE, bool HAS_Z, int S, bool CONV = false, int FLAGS = 0>
+template <typename T, int MODE, bool HAS_Z, int S, bool CONV = false, int FLAGS = 0, bool LEAN = false>
 cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int grid_chunks,
                           cudaStream_t st) {
-    using Sh = TmShape<T, MODE, S, CONV>;
-    auto kern = scan_tm_kernel<T, MODE, HAS_Z, S, CONV, FLAGS>;
+    using Sh = TmShape<T, MODE, S, CONV, LEAN>;
+    // registers of a full-width CTA: the warps on the busiest sub-partition fit its quarter of the file
+    static_assert((Sh::MAX_WARPS + 1 + 3) / 4 * 32 * (LEAN ? 96 : 168) <= 16384, "registers of a full-width CTA");
+    void (*kern)(const ScanArgs, const TmMaps) = nullptr;
+    if constexpr (LEAN) kern = scan_tm_lean_kernel<T, MODE, HAS_Z, S>;
+    else kern = scan_tm_kernel<T, MODE, HAS_Z, S, CONV, FLAGS>;
     static bool attr_set[kMaxDevices] = {};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -684,6 +722,13 @@ cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, int warps, long
     dim3 grid((unsigned)((a.Dch + ch - 1) / ch), (unsigned)Bsz, (unsigned)grid_chunks);
     kern<<<grid, 32 * (warps + 1), Sh::SMEM_BYTES, st>>>(a, maps);  // + the producer warp
     return cudaGetLastError();
+}
+
+// The lean form (12..18 compute warps) of the plain direct scan, bf16 storage.
+template <int S>
+cudaError_t launch_tm_lean(const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, cudaStream_t st) {
+    return a.z != nullptr ? launch_tm_one<bf16_t, MODE_FULL, true, S, false, 0, true>(a, maps, warps, Bsz, 1, st)
+                          : launch_tm_one<bf16_t, MODE_FULL, false, S, false, 0, true>(a, maps, warps, Bsz, 1, st);
 }
 
 template <typename T, int S, int FLAGS = 0>

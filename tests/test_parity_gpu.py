@@ -373,3 +373,29 @@ def test_chunked_scan_correction_regimes(regime, io, scheme, monkeypatch):
         yr, hr = run_oracle(x, softplus=softplus, h0=None if h is None else h.astype(np.float64))
         assert_close(yg, yr, TOL_Y[io], f"{regime} {io} h0={h is not None} y")
         assert_close(hg, hr, TOL_STATE, f"{regime} {io} last_state")
+
+
+# ----------------------------------------------------------------------------- lean form: 12..18 compute warps
+
+@pytest.mark.parametrize("N", [12, 16, 32, 64])
+@pytest.mark.parametrize("with_z", [True, False])
+def test_lean_form_forced(N, with_z, monkeypatch):
+    """MAMBA_TM_LEAN=1 puts every plain, aligned, direct bf16 scan on the lean form of the tensor-memory
+    kernel (one step pair's TMEM columns at a time, 12..18 compute warps per CTA): ragged channel tiles,
+    a ragged time tail, every element against the oracle."""
+    monkeypatch.setenv("MAMBA_TM_LEAN", "1")
+    x = inputs.make_scan_inputs(2, 300, N, 1000, io="bf16", seed=60 + N)
+    check(x, f"lean N={N} z={with_z}", with_z=with_z)
+    # softplus off: Delta = Delta_raw + bias must stay positive for a decaying state
+    x.delta_bias = (x.delta_bias * 0 + 2.0).astype(np.float32)
+    check(x, f"lean N={N} z={with_z} no softplus, no D", with_z=with_z, softplus=False, with_D=False)
+
+
+@pytest.mark.parametrize("N,Dch", [(16, 21000), (32, 10600), (64, 5300)])
+def test_lean_form_widest_cta_chosen_automatically(N, Dch):
+    """Channel counts for which only the widest lean CTA (18 compute warps) fits the batch in one wave of
+    148 SMs, where the regular 8..11-warp CTAs need two: the automatic choice takes the lean form at
+    W = 18, 19 warps per CTA, 5 on some SM sub-partitions (ragged last CTA, ragged time tail; 16-byte
+    aligned rows, so the tensor-memory kernel serves it)."""
+    x = inputs.make_scan_inputs(1, Dch, N, 200, io="bf16", seed=70 + N)
+    check(x, f"lean widest N={N} Dch={Dch}")
