@@ -85,3 +85,12 @@ def test_backward_long_rows():
     """Rows of the 130M-shaped layer's length (L = 2048, bf16) over 96 channels, every output against the oracle."""
     x = inputs.make_scan_inputs(1, 96, 16, 2048, io="bf16", seed=400)
     check_bwd(x, "bwd L=2048 D=96", seed=4)
+
+
+def test_backward_full_130m_layer_every_element():
+    """The whole 130M-shaped layer (B8 D1536 N16 L2048, bf16), in the launch configuration the benchmark
+    times: every du, ddelta, dz element and every dA, dB, dC, dD, ddelta_bias sum against the oracle."""
+    x = inputs.make_workload("mamba130m_b8_d1536_n16_l2048_bf16")
+    check_bwd(x, "bwd 130M layer", seed=5)
+    assert m.mamba_device_error() == 0
+
