@@ -324,6 +324,8 @@ def main():
         }
         if res.get("chained") is not None:
             line["chained"] = res["chained"]
+        if res.get("training_pair") is not None:
+            line["training_pair"] = res["training_pair"]
         if extra is not None:
             line["workloads"] = extra
         print(json.dumps(line))
@@ -346,6 +348,8 @@ def workload_entry(res):
          "gpu_launches": res["launches"]}
     if res.get("chained") is not None:
         e["chained"] = res["chained"]
+    if res.get("training_pair") is not None:
+        e["training_pair"] = res["training_pair"]
     return e
 
 
@@ -807,8 +811,46 @@ def bench_backward(args, m, torch, workload=None, steps=None, e2e=True):
         ev1.record(stream)
         torch.cuda.synchronize()
     t_ms = ev0.elapsed_time(ev1) / steps
-
     clocks = cs.summary()
+
+    # the training pair: the forward scan that saves the checkpoints, then the backward that starts from them
+    ckb = m.mamba_scan_bwd_ckpt_size(Bsz, Dch, L, N)
+    cks = [torch.empty(ckb // 4, **f32) for _ in range(R)]
+    ys = [torch.empty_like(t["u"]) for _ in range(R)]
+
+    def fwd_save(i):
+        s = sets[i % R]
+        m.mamba_selective_scan_fwd_save(s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, ys[i % R], None,
+                                        cks[i % R], stream=stream)
+
+    def bwd_ckpt(i):
+        s, o = sets[i % R], outs[i % R]
+        m.mamba_selective_scan_bwd_from_ckpt(s["u"], s["delta"], A, s["B"], s["C"], D, s["z"], bias, 1, s["dy"],
+                                             cks[i % R], o["du"], o["dd"], o["dA"], o["dB"], o["dC"], o["dD"], o["dz"],
+                                             o["db"], stream=stream)
+
+    def timed(fn, n):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n):
+            fn(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    for i in range(R):      # every rotating set holds its own checkpoints
+        fwd_save(i)
+    fs_ms = timed(fwd_save, steps)
+    bc_ms = timed(bwd_ckpt, steps)
+    training_pair = {"fwd_save_ms": round(fs_ms, 6), "bwd_from_ckpt_ms": round(bc_ms, 6),
+                     "ckpt_bytes": ckb,
+                     "note": "mamba_selective_scan_fwd_save (the direct scan writing the backward's checkpoints) "
+                             "and mamba_selective_scan_bwd_from_ckpt (no checkpoint sweep), each timed alone"}
+    del cks, ys
+
     e2e_ms, h2d, d2h = None, None, None
     if e2e:
         e2e_ms, h2d, d2h = bwd_e2e(args, torch, t, sets, outs, step, stream)
@@ -832,7 +874,8 @@ def bench_backward(args, m, torch, workload=None, steps=None, e2e=True):
                         "l2": f"inputs rotate over {R} resident copies"},
                 roofline=roof, h2d=h2d, d2h=d2h, e2e_ms=e2e_ms,
                 launches=steps,  # the backward kernel (plus five cudaMemsetAsync zero fills per step)
-                clocks=clocks, inputs=x, mufu={"ex2_per_clk_per_sm": round(mufu_per_clk, 3), "sms": sms})
+                clocks=clocks, inputs=x, mufu={"ex2_per_clk_per_sm": round(mufu_per_clk, 3), "sms": sms},
+                training_pair=training_pair)
 
 
 def bwd_e2e(args, torch, t, sets, outs, step, stream):

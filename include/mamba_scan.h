@@ -179,9 +179,11 @@ int mamba_state_update(float *state, const void *u, const void *delta, const flo
  *   dz          [Bsz][Dch][L] (dtype), required when z is given (else ignored)
  *   dA [Dch][N], dB, dC [Bsz][N][L], dD [Dch], ddelta_bias [Dch]: fp32 sums,
  *               written from zero by the call (dD, ddelta_bias may be NULL)
- * States are recomputed from checkpoints taken every few steps; the
- * checkpoints (Bsz*Dch*ceil(L/c)*N*4 bytes, c = 8, 4 or 2 for N <= 16, 32, 64)
- * are allocated and freed stream-ordered inside the call.  dB and dC receive
+ * States are recomputed from checkpoints taken every c steps (c = 16, 8 or 4
+ * for N <= 16, 32, 64); this call first sweeps the sequence forwards to take
+ * them, in a workspace of mamba_scan_bwd_ckpt_size(...) bytes allocated and
+ * freed stream-ordered inside the call (mamba_selective_scan_fwd_save and
+ * mamba_selective_scan_bwd_from_ckpt below skip that sweep).  dB and dC receive
  * atomic additions, so their low-order bits may vary between runs.  Returns
  * MAMBA_OK, MAMBA_ERR_NULL_ARG, MAMBA_ERR_BAD_SHAPE, MAMBA_ERR_UNSUPPORTED_N,
  * MAMBA_ERR_BAD_DTYPE, MAMBA_ERR_ALLOC or MAMBA_ERR_LAUNCH.
@@ -191,6 +193,43 @@ int mamba_selective_scan_bwd(const void *u, const void *delta, const float *A, c
                              const void *dy, void *du, void *ddelta, float *dA, float *dB, float *dC, float *dD,
                              void *dz, float *ddelta_bias, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
                              int dtype, mamba_stream_t stream);
+
+/*
+ * Training pair: a forward scan that also saves the backward pass's
+ * checkpoints, and a backward pass that starts from them instead of sweeping
+ * the sequence forwards again (the same gradients as mamba_selective_scan_bwd,
+ * up to rounding).  No counterpart on the pages, which measure training
+ * throughput but print no backward pass: the checkpoints are this library's
+ * layout.
+ *
+ * mamba_scan_bwd_ckpt_size: bytes of the checkpoint buffer,
+ *   Bsz*Dch*K*P*4 with c = 16, 8, 4 steps and P = 16, 32, 64 padded states for
+ *   N <= 16, 32, 64, and K = ceil(L / c); 0 for invalid sizes.
+ * mamba_selective_scan_fwd_save: mamba_selective_scan_fwd as the direct
+ *   (single-pass) scan, plus ckpt [Bsz][Dch][K][P] fp32, caller-owned device
+ *   memory, 16-byte aligned: entry k (1 <= k < K) receives the state before
+ *   step k*c, zero past N; entry 0 is not written.  On 16-byte aligned rows
+ *   with 8 < N <= 64 (fp32: N <= 16) the tensor-memory scan writes them as it
+ *   goes; otherwise the scan runs and then one more kernel sweeps the
+ *   sequence for them.
+ * mamba_selective_scan_bwd_from_ckpt: the arguments of mamba_selective_scan_bwd
+ *   plus ckpt as written by mamba_selective_scan_fwd_save for the same inputs
+ *   (read only; no workspace is allocated).
+ * Both return MAMBA_OK, MAMBA_ERR_NULL_ARG, MAMBA_ERR_BAD_SHAPE (also for a
+ * misaligned ckpt), MAMBA_ERR_UNSUPPORTED_N, MAMBA_ERR_BAD_DTYPE or
+ * MAMBA_ERR_LAUNCH.
+ */
+size_t mamba_scan_bwd_ckpt_size(int64_t Bsz, int64_t Dch, int64_t L, int64_t N);
+int mamba_selective_scan_fwd_save(const void *u, const void *delta, const float *A, const void *B,
+                                  const void *C, const float *D, const void *z, const float *delta_bias,
+                                  int softplus_flag, void *y, float *last_state, float *ckpt, int64_t Bsz,
+                                  int64_t Dch, int64_t L, int64_t N, int dtype, mamba_stream_t stream);
+int mamba_selective_scan_bwd_from_ckpt(const void *u, const void *delta, const float *A, const void *B,
+                                       const void *C, const float *D, const void *z, const float *delta_bias,
+                                       int softplus_flag, const void *dy, const float *ckpt, void *du,
+                                       void *ddelta, float *dA, float *dB, float *dC, float *dD, void *dz,
+                                       float *ddelta_bias, int64_t Bsz, int64_t Dch, int64_t L, int64_t N,
+                                       int dtype, mamba_stream_t stream);
 
 /*
  * Depthwise causal convolution of width 4 followed by SiLU -- the branch that

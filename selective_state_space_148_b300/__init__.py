@@ -70,6 +70,12 @@ def lib() -> ctypes.CDLL:
                                                     i64, i64, ci, vp]
         L.mamba_selective_scan_bwd.restype = ci
         L.mamba_selective_scan_bwd.argtypes = [vp] * 8 + [ci] + [vp] * 9 + [i64] * 4 + [ci, vp]
+        L.mamba_scan_bwd_ckpt_size.restype = sz
+        L.mamba_scan_bwd_ckpt_size.argtypes = [i64] * 4
+        L.mamba_selective_scan_fwd_save.restype = ci
+        L.mamba_selective_scan_fwd_save.argtypes = [vp] * 8 + [ci] + [vp] * 3 + [i64] * 4 + [ci, vp]
+        L.mamba_selective_scan_bwd_from_ckpt.restype = ci
+        L.mamba_selective_scan_bwd_from_ckpt.argtypes = [vp] * 8 + [ci] + [vp] * 10 + [i64] * 4 + [ci, vp]
         L.mamba_bench_ex2.restype = ci
         L.mamba_bench_ex2.argtypes = [vp, vp, i64, ci, ci, vp]
         _lib = L
@@ -179,6 +185,39 @@ def mamba_selective_scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag,
                                         _ptr(dA), _ptr(dB), _ptr(dC), _ptr(dD), _ptr(dz), _ptr(ddelta_bias),
                                         Bsz, Dch, L, N, _dtype_code(u), _stream(stream))
     _check(st, "mamba_selective_scan_bwd")
+
+
+def mamba_scan_bwd_ckpt_size(Bsz, Dch, L, N) -> int:
+    """Bytes of the checkpoint buffer of mamba_selective_scan_fwd_save / mamba_selective_scan_bwd_from_ckpt."""
+    n = lib().mamba_scan_bwd_ckpt_size(int(Bsz), int(Dch), int(L), int(N))
+    if n == 0:
+        raise MambaError(-2, "mamba_scan_bwd_ckpt_size")
+    return int(n)
+
+
+def mamba_selective_scan_fwd_save(u, delta, A, B, C, D, z, delta_bias, softplus_flag, y, last_state, ckpt,
+                                  stream=None):
+    """The direct forward scan that also writes the backward pass's checkpoints into ckpt (fp32, at least
+    mamba_scan_bwd_ckpt_size bytes)."""
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    st = lib().mamba_selective_scan_fwd_save(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                             _ptr(delta_bias), int(bool(softplus_flag)), _ptr(y), _ptr(last_state),
+                                             _ptr(ckpt), Bsz, Dch, L, N, _dtype_code(u), _stream(stream))
+    _check(st, "mamba_selective_scan_fwd_save")
+
+
+def mamba_selective_scan_bwd_from_ckpt(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, ckpt, du, ddelta, dA,
+                                       dB, dC, dD, dz, ddelta_bias, stream=None):
+    """mamba_selective_scan_bwd starting from the checkpoints mamba_selective_scan_fwd_save wrote."""
+    Bsz, Dch, L = u.shape
+    N = A.shape[1]
+    st = lib().mamba_selective_scan_bwd_from_ckpt(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                                  _ptr(delta_bias), int(bool(softplus_flag)), _ptr(dy), _ptr(ckpt),
+                                                  _ptr(du), _ptr(ddelta), _ptr(dA), _ptr(dB), _ptr(dC), _ptr(dD),
+                                                  _ptr(dz), _ptr(ddelta_bias), Bsz, Dch, L, N, _dtype_code(u),
+                                                  _stream(stream))
+    _check(st, "mamba_selective_scan_bwd_from_ckpt")
 
 
 def mamba_scan_workspace_size(Bsz, Dch, L, N, chunk_len=0, dtype=MAMBA_BF16) -> int:

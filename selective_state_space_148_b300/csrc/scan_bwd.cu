@@ -46,10 +46,12 @@ struct BwdArgs {
     const float *A, *D, *bias;
     void *du, *ddelta, *dz;
     float *dA, *dB, *dC, *dD, *dbias;
-    float *ckpt;  // [Bsz][Dch][K][NP]: the state before step k * TC
+    float *ckpt;  // [Bsz][Dch][K][NP]: the state before step k * TC (entry 0 unused)
     long long Dch, L, N;
     int softplus;
     int vec;  // L % 4 == 0 and every row pointer 16-byte aligned: vector loads, stores and atomics
+    int ckpt_given;  // 1: the checkpoints were saved by the forward pass (no checkpoint sweep here)
+    int sweep_only;  // 1: only the checkpoint sweep, writing every entry 1 .. K-1, then return
 };
 
 template <int NS>
@@ -246,15 +248,25 @@ scan_bwd_kernel(const BwdArgs a, int K) {
     Pack<T, 4> pbc;              // this thread's 4 steps of its B or C row (one chunk ahead)
 
     // ---- forward sweep over chunks 0 .. K-2: the state before each chunk k >= 1 goes to the checkpoints
+    // (skipped when the forward pass saved them)
     float2 h2[NH];
 #pragma unroll
     for (int jp = 0; jp < NH; ++jp) h2[jp] = f2(0.f, 0.f);
-    if (K > 1) {
+    if (a.ckpt_given) {
+        if (K > 1 && valid) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+                const float4 v = *reinterpret_cast<const float4 *>(ck + (long long)(K - 1) * NP + 4 * q);
+                h2[2 * q] = f2(v.x, v.y);
+                h2[2 * q + 1] = f2(v.z, v.w);
+            }
+        }
+    } else if (K > 1) {
         pu.load(a.u, row + s * G, lane_valid(0), vec);
         pr.load(a.delta, row + s * G, lane_valid(0), vec);
         if (rwhich == 0) pbc.load(a.Bm, bcrow + 4 * rg, row_valid(0), vec);
     }
-    for (int k = 0; k + 1 < K; ++k) {
+    for (int k = 0; !a.ckpt_given && k + 1 < K; ++k) {
         const long long t0 = (long long)k * TC;
         __syncthreads();  // the previous chunk's readers are done
 #pragma unroll
@@ -298,6 +310,15 @@ scan_bwd_kernel(const BwdArgs a, int K) {
         }
     }
     // h2 now holds the state before the last chunk
+    if (a.sweep_only) {  // (uniform over the grid: every thread returns here)
+        if (K > 1 && valid) {
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+                *reinterpret_cast<float4 *>(ck + (long long)(K - 1) * NP + 4 * q) =
+                    make_float4(h2[2 * q].x, h2[2 * q].y, h2[2 * q + 1].x, h2[2 * q + 1].y);
+        }
+        return;
+    }
 
     // ---- reverse sweep, chunk by chunk
     float2 dh2[NH], dA2[NH];
@@ -530,74 +551,178 @@ cudaError_t launch_scan_bwd(int dtype, const BwdArgs &a, long long Bsz, cudaStre
 
 // ---------------------------------------------------------------------------- C ABI
 
-extern "C" int mamba_selective_scan_bwd(const void *u, const void *delta, const float *A, const void *B,
-                                        const void *C, const float *D, const void *z, const float *delta_bias,
-                                        int softplus_flag, const void *dy, void *du, void *ddelta, float *dA,
-                                        float *dB, float *dC, float *dD, void *dz, float *ddelta_bias, int64_t Bsz,
-                                        int64_t Dch, int64_t L, int64_t N, int dtype, mamba_stream_t stream) {
-    using namespace mamba;
-    if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC) return MAMBA_ERR_NULL_ARG;
-    if (z != nullptr && dz == nullptr) return MAMBA_ERR_NULL_ARG;
+namespace {
+
+using namespace mamba;
+
+// Shape checks shared by the entry points (the checkpoint chunks are at least 4 steps).
+int check_bwd_shape(int64_t Bsz, int64_t Dch, int64_t L, int64_t N, int dtype) {
     if (dtype != MAMBA_F32 && dtype != MAMBA_BF16) return MAMBA_ERR_BAD_DTYPE;
     constexpr long long kMax = 1LL << 40;
-    const long long Kc = (L + 3) / 4;  // checkpoint chunks are at least 4 steps
+    const long long Kc = (L + 3) / 4;
     if (Bsz <= 0 || Dch <= 0 || L <= 0 || N <= 0 || Bsz > 65535 || Dch > kMax || L > kMax ||
         Bsz * Dch > kMax / L || Bsz * N > kMax / L || Bsz * Dch > kMax / (Kc * 64) || Kc > (1LL << 30))
         return MAMBA_ERR_BAD_SHAPE;
     if (N > 64) return MAMBA_ERR_UNSUPPORTED_N;
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    return MAMBA_OK;
+}
+
+size_t ckpt_bytes(int64_t Bsz, int64_t Dch, int64_t L, int64_t N) {
     const long long K = (L + bwd_chunk_steps(N) - 1) / bwd_chunk_steps(N);
-    const long long NP = 4LL * bwd_ns(N);
-    const size_t ck_bytes = (size_t)(Bsz * Dch) * (size_t)K * (size_t)NP * sizeof(float);
-    void *ck = nullptr;
-    const char *inject = std::getenv("MAMBA_FAULT_INJECT");  // host-side test hook, as in the forward scan
-    if (inject != nullptr && std::strcmp(inject, "alloc") == 0) return MAMBA_ERR_ALLOC;
-    if (cudaMallocAsync(&ck, ck_bytes, st) != cudaSuccess) {
-        cudaGetLastError();
-        return MAMBA_ERR_ALLOC;
-    }
-    int rc = MAMBA_OK;
+    return (size_t)(Bsz * Dch) * (size_t)K * (size_t)(4LL * bwd_ns(N)) * sizeof(float);
+}
+
+bool aligned16(const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The backward kernel over caller-provided (given = 1) or call-owned checkpoints.
+int run_bwd(const void *u, const void *delta, const float *A, const void *B, const void *C, const float *D,
+            const void *z, const float *delta_bias, int softplus_flag, const void *dy, void *du, void *ddelta,
+            float *dA, float *dB, float *dC, float *dD, void *dz, float *ddelta_bias, int64_t Bsz, int64_t Dch,
+            int64_t L, int64_t N, int dtype, cudaStream_t st, float *ck, int given) {
     // the sums start from zero
     if (cudaMemsetAsync(dA, 0, (size_t)(Dch * N) * sizeof(float), st) != cudaSuccess ||
         cudaMemsetAsync(dB, 0, (size_t)(Bsz * N * L) * sizeof(float), st) != cudaSuccess ||
         cudaMemsetAsync(dC, 0, (size_t)(Bsz * N * L) * sizeof(float), st) != cudaSuccess ||
         (dD != nullptr && cudaMemsetAsync(dD, 0, (size_t)Dch * sizeof(float), st) != cudaSuccess) ||
         (ddelta_bias != nullptr && cudaMemsetAsync(ddelta_bias, 0, (size_t)Dch * sizeof(float), st) != cudaSuccess))
-        rc = MAMBA_ERR_LAUNCH;
-    if (rc == MAMBA_OK) {
-        BwdArgs a{};
-        a.u = u;
-        a.delta = delta;
-        a.z = z;
-        a.Bm = B;
-        a.Cm = C;
-        a.dy = dy;
-        a.A = A;
-        a.D = D;
-        a.bias = delta_bias;
-        a.du = du;
-        a.ddelta = ddelta;
-        a.dz = dz;
-        a.dA = dA;
-        a.dB = dB;
-        a.dC = dC;
-        a.dD = dD;
-        a.dbias = ddelta_bias;
-        a.ckpt = static_cast<float *>(ck);
-        a.Dch = Dch;
-        a.L = L;
-        a.N = N;
-        a.softplus = softplus_flag ? 1 : 0;
-        auto al16 = [](const void *p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-        a.vec = (L % 4 == 0 && al16(u) && al16(delta) && al16(z) && al16(B) && al16(C) && al16(dy) && al16(du) &&
-                 al16(ddelta) && al16(dz) && al16(dB) && al16(dC))
-                    ? 1
-                    : 0;
-        if (launch_scan_bwd(dtype, a, Bsz, st) != cudaSuccess) rc = MAMBA_ERR_LAUNCH;
+        return MAMBA_ERR_LAUNCH;
+    BwdArgs a{};
+    a.u = u;
+    a.delta = delta;
+    a.z = z;
+    a.Bm = B;
+    a.Cm = C;
+    a.dy = dy;
+    a.A = A;
+    a.D = D;
+    a.bias = delta_bias;
+    a.du = du;
+    a.ddelta = ddelta;
+    a.dz = dz;
+    a.dA = dA;
+    a.dB = dB;
+    a.dC = dC;
+    a.dD = dD;
+    a.dbias = ddelta_bias;
+    a.ckpt = ck;
+    a.ckpt_given = given;
+    a.Dch = Dch;
+    a.L = L;
+    a.N = N;
+    a.softplus = softplus_flag ? 1 : 0;
+    a.vec = (L % 4 == 0 && aligned16(u) && aligned16(delta) && aligned16(z) && aligned16(B) && aligned16(C) &&
+             aligned16(dy) && aligned16(du) && aligned16(ddelta) && aligned16(dz) && aligned16(dB) && aligned16(dC))
+                ? 1
+                : 0;
+    return launch_scan_bwd(dtype, a, Bsz, st) == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" size_t mamba_scan_bwd_ckpt_size(int64_t Bsz, int64_t Dch, int64_t L, int64_t N) {
+    if (check_bwd_shape(Bsz, Dch, L, N, MAMBA_F32) != MAMBA_OK) return 0;
+    return ckpt_bytes(Bsz, Dch, L, N);
+}
+
+extern "C" int mamba_selective_scan_bwd(const void *u, const void *delta, const float *A, const void *B,
+                                        const void *C, const float *D, const void *z, const float *delta_bias,
+                                        int softplus_flag, const void *dy, void *du, void *ddelta, float *dA,
+                                        float *dB, float *dC, float *dD, void *dz, float *ddelta_bias, int64_t Bsz,
+                                        int64_t Dch, int64_t L, int64_t N, int dtype, mamba_stream_t stream) {
+    if (!u || !delta || !A || !B || !C || !dy || !du || !ddelta || !dA || !dB || !dC) return MAMBA_ERR_NULL_ARG;
+    if (z != nullptr && dz == nullptr) return MAMBA_ERR_NULL_ARG;
+    int rc = check_bwd_shape(Bsz, Dch, L, N, dtype);
+    if (rc != MAMBA_OK) return rc;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    void *ck = nullptr;
+    const char *inject = std::getenv("MAMBA_FAULT_INJECT");  // host-side test hook, as in the forward scan
+    if (inject != nullptr && std::strcmp(inject, "alloc") == 0) return MAMBA_ERR_ALLOC;
+    if (cudaMallocAsync(&ck, ckpt_bytes(Bsz, Dch, L, N), st) != cudaSuccess) {
+        cudaGetLastError();
+        return MAMBA_ERR_ALLOC;
     }
+    rc = run_bwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, ddelta, dA, dB, dC, dD, dz,
+                 ddelta_bias, Bsz, Dch, L, N, dtype, st, static_cast<float *>(ck), 0);
     if (cudaFreeAsync(ck, st) != cudaSuccess) {
         cudaGetLastError();
         if (rc == MAMBA_OK) rc = MAMBA_ERR_LAUNCH;
     }
     return rc;
+}
+
+extern "C" int mamba_selective_scan_bwd_from_ckpt(const void *u, const void *delta, const float *A, const void *B,
+                                                  const void *C, const float *D, const void *z,
+                                                  const float *delta_bias, int softplus_flag, const void *dy,
+                                                  const float *ckpt, void *du, void *ddelta, float *dA, float *dB,
+                                                  float *dC, float *dD, void *dz, float *ddelta_bias, int64_t Bsz,
+                                                  int64_t Dch, int64_t L, int64_t N, int dtype,
+                                                  mamba_stream_t stream) {
+    if (!u || !delta || !A || !B || !C || !dy || !ckpt || !du || !ddelta || !dA || !dB || !dC)
+        return MAMBA_ERR_NULL_ARG;
+    if (z != nullptr && dz == nullptr) return MAMBA_ERR_NULL_ARG;
+    const int rc = check_bwd_shape(Bsz, Dch, L, N, dtype);
+    if (rc != MAMBA_OK) return rc;
+    if (!aligned16(ckpt)) return MAMBA_ERR_BAD_SHAPE;
+    // the kernel only reads the checkpoints in this mode
+    return run_bwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dy, du, ddelta, dA, dB, dC, dD, dz,
+                   ddelta_bias, Bsz, Dch, L, N, dtype, reinterpret_cast<cudaStream_t>(stream),
+                   const_cast<float *>(ckpt), 1);
+}
+
+extern "C" int mamba_selective_scan_fwd_save(const void *u, const void *delta, const float *A, const void *B,
+                                             const void *C, const float *D, const void *z,
+                                             const float *delta_bias, int softplus_flag, void *y,
+                                             float *last_state, float *ckpt, int64_t Bsz, int64_t Dch, int64_t L,
+                                             int64_t N, int dtype, mamba_stream_t stream) {
+    if (!u || !delta || !A || !B || !C || !y || !ckpt) return MAMBA_ERR_NULL_ARG;
+    const int rc = check_bwd_shape(Bsz, Dch, L, N, dtype);
+    if (rc != MAMBA_OK) return rc;
+    if (!aligned16(ckpt)) return MAMBA_ERR_BAD_SHAPE;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int es = dtype == MAMBA_BF16 ? 2 : 4;
+    const bool vec = aligned16(u) && aligned16(delta) && aligned16(B) && aligned16(C) && aligned16(y) &&
+                     aligned16(z) && (L * es) % 16 == 0;
+    ScanArgs a{};
+    a.u = u;
+    a.delta = delta;
+    a.z = z;
+    a.Bm = B;
+    a.Cm = C;
+    a.A = A;
+    a.D = D;
+    a.bias = delta_bias;
+    a.y = y;
+    a.last_state = last_state;
+    a.Dch = Dch;
+    a.L = L;
+    a.N = N;
+    a.softplus = softplus_flag ? 1 : 0;
+    a.chunk_len = L;
+    a.nchunks = 1;
+    // the direct scan on the tensor-memory kernel writes the checkpoints as it goes
+    if (vec && tm_kernel_for(dtype, N)) {
+        a.ckpt = ckpt;
+        a.ckpt_k = (int)((L + bwd_chunk_steps(N) - 1) / bwd_chunk_steps(N));
+        const cudaError_t e = launch_scan_tm(dtype, MODE_FULL, a, Bsz, 1, st);
+        if (e == cudaSuccess) return MAMBA_OK;
+        if (e != cudaErrorNotSupported) return MAMBA_ERR_LAUNCH;
+        a.ckpt = nullptr;
+    }
+    // otherwise: the direct scan, then the backward kernel's own checkpoint sweep
+    if (launch_scan(dtype, MODE_FULL, vec, a, Bsz, 1, st) != cudaSuccess) return MAMBA_ERR_LAUNCH;
+    BwdArgs b{};
+    b.u = u;
+    b.delta = delta;
+    b.Bm = B;
+    b.Cm = C;
+    b.A = A;
+    b.bias = delta_bias;
+    b.ckpt = ckpt;
+    b.Dch = Dch;
+    b.L = L;
+    b.N = N;
+    b.softplus = softplus_flag ? 1 : 0;
+    b.vec = (L % 4 == 0 && aligned16(u) && aligned16(delta) && aligned16(B)) ? 1 : 0;
+    b.sweep_only = 1;
+    return launch_scan_bwd(dtype, b, Bsz, st) == cudaSuccess ? MAMBA_OK : MAMBA_ERR_LAUNCH;
 }

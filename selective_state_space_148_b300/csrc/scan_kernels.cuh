@@ -62,6 +62,10 @@ struct ScanArgs {
     // the kernel (tensor-memory kernel only): taps [Dch][4], bias [Dch] or null
     const float *conv_w, *conv_b;
     int chunk0;  // MODE_CORR: chunk of blockIdx.z == 0
+    // tensor-memory kernel, plain direct scan: non-null = also write the backward pass's checkpoints,
+    // [Bsz][Dch][ckpt_k][4 S] (S lanes per channel): entry k >= 1 is the state before step k * 64 / S
+    float *ckpt;
+    int ckpt_k;
 };
 
 enum { SCAN_FLAG_ZOH = 1, SCAN_FLAG_REVERSE = 2 };

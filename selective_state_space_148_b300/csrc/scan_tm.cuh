@@ -601,6 +601,16 @@ __device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &ma
                         hh[j].x = fmaf(e.x, hh[j].y, bu.x);
                         hh[j].y = fmaf(e.y, hh[j].x, bu.y);
                     }
+                    // the backward pass's checkpoint: the state before step k * TCK, every TCK = 64 / S steps
+                    // (the chunk length of the backward kernel for this state count)
+                    if constexpr (MODE == MODE_FULL && FLAGS == 0 && !CONV) {
+                        if ((q * TB + 2 * p + 2) % (64 / S) == 0 && a.ckpt != nullptr && valid) {  // q, p unrolled
+                            const long long kc = ((long long)sup * TT + q * TB + 2 * p + 2) / (64 / S);
+                            if (kc < a.ckpt_k)
+                                *reinterpret_cast<float4 *>(a.ckpt + ((b * a.Dch + d) * a.ckpt_k + kc) * (4 * S) + 4 * s) =
+                                    make_float4(hh[0].y, hh[1].y, hh[2].y, hh[3].y);
+                        }
+                    }
                     if (HASY) {
                         float2 P = __fmul2_rn(f2(__uint_as_float(ccp[0]), __uint_as_float(ccp[1])), hh[0]);
                         P = __ffma2_rn(f2(__uint_as_float(ccp[2]), __uint_as_float(ccp[3])), hh[1], P);

@@ -100,3 +100,33 @@ def test_bench_validation():
     assert L.mamba_bench_ex2(None, FAKE, 10, 1, 32, None) == -1
     assert L.mamba_bench_ex2(FAKE, FAKE, 0, 1, 32, None) == -2
     assert L.mamba_bench_ex2(FAKE, FAKE, 10, 1, 2048, None) == -2
+
+
+def test_training_pair_host_checks():
+    """Checkpoint buffer sizes and the host-side argument checks of the forward-with-checkpoints and
+    backward-from-checkpoints entry points (no GPU: every call fails validation first)."""
+    L = m.lib()
+    # Bsz * Dch * ceil(L / c) * P * 4 bytes with (c, P) = (16, 16), (8, 32), (4, 64) for N <= 16, 32, 64
+    assert L.mamba_scan_bwd_ckpt_size(8, 1536, 2048, 16) == 8 * 1536 * 128 * 16 * 4
+    assert L.mamba_scan_bwd_ckpt_size(2, 3, 17, 32) == 2 * 3 * 3 * 32 * 4
+    assert L.mamba_scan_bwd_ckpt_size(1, 1, 5, 64) == 1 * 1 * 2 * 64 * 4
+    assert L.mamba_scan_bwd_ckpt_size(1, 1, 5, 65) == 0
+    assert L.mamba_scan_bwd_ckpt_size(0, 1, 5, 16) == 0
+
+    def fwd(ck, N=16, dt=m.MAMBA_BF16, y=FAKE):
+        return L.mamba_selective_scan_fwd_save(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 1, y, None, ck, 1, 4, 64,
+                                               N, dt, None)
+
+    def bwd(ck, N=16):
+        return L.mamba_selective_scan_bwd_from_ckpt(FAKE, FAKE, FAKE, FAKE, FAKE, None, None, None, 1, FAKE, ck, FAKE,
+                                                    FAKE, FAKE, FAKE, FAKE, None, None, None, 1, 4, 64, N,
+                                                    m.MAMBA_BF16, None)
+
+    assert fwd(None) == m.STATUS_CODE["MAMBA_ERR_NULL_ARG"]
+    assert fwd(FAKE, y=None) == m.STATUS_CODE["MAMBA_ERR_NULL_ARG"]
+    assert fwd(FAKE + 4) == m.STATUS_CODE["MAMBA_ERR_BAD_SHAPE"]        # checkpoints must be 16-byte aligned
+    assert fwd(FAKE, N=65) == m.STATUS_CODE["MAMBA_ERR_UNSUPPORTED_N"]
+    assert fwd(FAKE, dt=7) == m.STATUS_CODE["MAMBA_ERR_BAD_DTYPE"]
+    assert bwd(None) == m.STATUS_CODE["MAMBA_ERR_NULL_ARG"]
+    assert bwd(FAKE + 4) == m.STATUS_CODE["MAMBA_ERR_BAD_SHAPE"]
+    assert bwd(FAKE, N=0) == m.STATUS_CODE["MAMBA_ERR_BAD_SHAPE"]
