@@ -91,25 +91,21 @@ __device__ __forceinline__ float zoh_weight(float e, float x2, float dl, float i
 
 // The same weight for a pair of steps of one state, in packed arithmetic:
 // f = Delta phi(Delta A), phi(y) = (e^y - 1) / y.  x = Delta A log2 e (the
-// decay's exponent), e = 2^x.  Where |Delta A| < 1/2, phi is its Taylor series
-// to the y^6 term (truncation below 2e-7 relative), written in x (coefficient k
-// is ln2^k / (k+1)!), so that A = 0 gives f = Delta with no special case;
-// elsewhere f = (e - 1) / A in one fused multiply-add (e * inv_a - inv_a, no
-// cancellation there).  inv_a = 1/A_n (anything finite where A_n = 0).
+// decay's exponent), e = 2^x.  Where |Delta A| < 1/64, phi is its Taylor series
+// to the y^2 term (the first dropped term, y^3/24, is below 2e-7 relative),
+// written in x (coefficient k is ln2^k / (k+1)!), so that A = 0 gives f = Delta
+// with no special case.  Elsewhere f = (e - 1) / A in one fused multiply-add
+// (e * inv_a - inv_a): there |e - 1| > 0.0155, so the ex2 error (about 2^-22
+// relative to e) is below 1.6e-5 of e - 1.  inv_a = 1/A_n (anything finite where
+// A_n = 0).
 __device__ __forceinline__ float2 zoh_weight2(float2 e, float2 x, float2 dl, float inv_a) {
     constexpr double l = 0.6931471805599453;
-    constexpr float c1 = (float)(l / 2), c2 = (float)(l * l / 6), c3 = (float)(l * l * l / 24);
-    constexpr float c4 = (float)(l * l * l * l / 120), c5 = (float)(l * l * l * l * l / 720);
-    constexpr float c6 = (float)(l * l * l * l * l * l / 5040);
-    float2 p = __ffma2_rn(x, f2(c6, c6), f2(c5, c5));
-    p = __ffma2_rn(x, p, f2(c4, c4));
-    p = __ffma2_rn(x, p, f2(c3, c3));
-    p = __ffma2_rn(x, p, f2(c2, c2));
-    p = __ffma2_rn(x, p, f2(c1, c1));
+    constexpr float c1 = (float)(l / 2), c2 = (float)(l * l / 6);
+    float2 p = __ffma2_rn(x, f2(c2, c2), f2(c1, c1));
     p = __ffma2_rn(x, p, f2(1.f, 1.f));
     const float2 small = __fmul2_rn(dl, p);
     const float2 big = __ffma2_rn(e, f2(inv_a, inv_a), f2(-inv_a, -inv_a));
-    constexpr float xmax = (float)(0.5 / l);  // |Delta A| < 1/2 in units of x
+    constexpr float xmax = (float)(1.0 / 64.0 / l);  // |Delta A| < 1/64 in units of x
     return f2(fabsf(x.x) < xmax ? small.x : big.x, fabsf(x.y) < xmax ? small.y : big.y);
 }
 

@@ -164,6 +164,10 @@ cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &args, long long 
                     encode_3d(&maps.B, a.Bm, bf16, a.L, a.N, Bsz, 4u * S, false) &&
                     encode_3d(&maps.C, a.Cm, bf16, a.L, a.N, Bsz, 4u * S, false);
     if (!ok) return cudaErrorNotSupported;
+    if (a.ckpt != nullptr) {  // the direct scan that also writes the backward's checkpoints
+        if (mode != MODE_FULL || grid_chunks != 1 || conv || a.flags != 0) return cudaErrorNotSupported;
+        return launch_tm_ckpt(dtype, S, a, maps, warps, lean_warps > 0, Bsz, st);
+    }
     if (mode == MODE_FULL_STATES || mode == MODE_CORR) {
         if (conv || a.flags != 0) return cudaErrorNotSupported;
         return launch_tm_chunk(dtype, S, mode, a, maps, warps, Bsz, grid_chunks, st);
@@ -193,12 +197,14 @@ cudaError_t launch_scan_tm(int dtype, int mode, const ScanArgs &args, long long 
 
 namespace mamba {
 int tm_read_clear_error(unsigned int *v) { return read_clear_word(g_device_error, v); }
+int tm_ckpt_read_clear_error(unsigned int *v);  // scan_tm_ckpt.cu
 }  // namespace mamba
 
 extern "C" int mamba_device_error(void) {
-    unsigned int v = 0, r = 0, z = 0, c = 0;
+    unsigned int v = 0, r = 0, z = 0, c = 0, k = 0;
     if (mamba::tm_read_clear_error(&v) != MAMBA_OK || mamba::tm_rev_read_clear_error(&r) != MAMBA_OK ||
-        mamba::tm_zoh_read_clear_error(&z) != MAMBA_OK || mamba::tm_chunk_read_clear_error(&c) != MAMBA_OK)
+        mamba::tm_zoh_read_clear_error(&z) != MAMBA_OK || mamba::tm_chunk_read_clear_error(&c) != MAMBA_OK ||
+        mamba::tm_ckpt_read_clear_error(&k) != MAMBA_OK)
         return MAMBA_ERR_DEVICE;
-    return (v | r | z | c) != 0 ? MAMBA_ERR_DEVICE_TIMEOUT : MAMBA_OK;
+    return (v | r | z | c | k) != 0 ? MAMBA_ERR_DEVICE_TIMEOUT : MAMBA_OK;
 }

@@ -80,7 +80,9 @@ struct TmMaps {
     CUtensorMap u, delta, z, B, C;
 };
 
-enum { FL_REV = 1, FL_ZOH = 2 };  // flag variants of the kernel (template argument FLAGS)
+// flag variants of the kernel (template argument FLAGS); FL_CKPT: the plain direct scan that also writes
+// the backward pass's checkpoints (ScanArgs::ckpt)
+enum { FL_REV = 1, FL_ZOH = 2, FL_CKPT = 4 };
 
 // S = lanes per channel (4, 8 or 16: N <= 4 S), each lane owning 4 states.
 // CONV: the first input tile is x with an 8-step halo (40 steps from t0 - 8,
@@ -143,7 +145,9 @@ struct TmShape {
 template <typename T, int MODE, bool HAS_Z, int S_, bool CONV, int FLAGS, bool LEAN>
 __device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &maps) {
     using Sh = TmShape<T, MODE, S_, CONV, LEAN>;
-    static_assert(!LEAN || (MODE == MODE_FULL && !CONV && FLAGS == 0), "the lean form serves the plain direct scan");
+    static_assert(!LEAN || (MODE == MODE_FULL && !CONV && (FLAGS == 0 || FLAGS == FL_CKPT)),
+                  "the lean form serves the plain direct scan");
+    static_assert(FLAGS != FL_CKPT || (MODE == MODE_FULL && !CONV), "checkpoints come from the plain direct scan");
     constexpr bool FAST = sizeof(T) == 2;
     constexpr bool HASY = MODE != MODE_STATES;                             // forms y (and reads C)
     constexpr bool ENDS = MODE == MODE_STATES || MODE == MODE_FULL_STATES;  // writes end states, sum of Delta
@@ -603,8 +607,8 @@ __device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &ma
                     }
                     // the backward pass's checkpoint: the state before step k * TCK, every TCK = 64 / S steps
                     // (the chunk length of the backward kernel for this state count)
-                    if constexpr (MODE == MODE_FULL && FLAGS == 0 && !CONV) {
-                        if ((q * TB + 2 * p + 2) % (64 / S) == 0 && a.ckpt != nullptr && valid) {  // q, p unrolled
+                    if constexpr (FLAGS == FL_CKPT) {
+                        if ((q * TB + 2 * p + 2) % (64 / S) == 0 && valid) {  // q, p unrolled: compile time
                             const long long kc = ((long long)sup * TT + q * TB + 2 * p + 2) / (64 / S);
                             if (kc < a.ckpt_k)
                                 *reinterpret_cast<float4 *>(a.ckpt + ((b * a.Dch + d) * a.ckpt_k + kc) * (4 * S) + 4 * s) =
@@ -703,9 +707,9 @@ scan_tm_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
 // The lean form: W = 12..18 compute warps and the producer warp; at most 96 registers per thread.  A
 // CTA's warps are spread over the SM's 4 sub-partitions, each with a quarter of the register file
 // (16 384 registers): 19 warps put 5 warps on a sub-partition, 5 x 32 x 96 = 15 360.
-template <typename T, int MODE, bool HAS_Z, int S_>
+template <typename T, int MODE, bool HAS_Z, int S_, int FLAGS = 0>
 __global__ void __maxnreg__(96) scan_tm_lean_kernel(const ScanArgs a, const __grid_constant__ TmMaps maps) {
-    scan_tm_body<T, MODE, HAS_Z, S_, false, 0, true>(a, maps);
+    scan_tm_body<T, MODE, HAS_Z, S_, false, FLAGS, true>(a, maps);
 }
 
 // Launch of one instantiation: grid (ceil(Dch / channels per CTA), Bsz, grid_chunks), W compute warps
@@ -717,7 +721,7 @@ cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, int warps, long
     // registers of a full-width CTA: the warps on the busiest sub-partition fit its quarter of the file
     static_assert((Sh::MAX_WARPS + 1 + 3) / 4 * 32 * (LEAN ? 96 : 168) <= 16384, "registers of a full-width CTA");
     void (*kern)(const ScanArgs, const TmMaps) = nullptr;
-    if constexpr (LEAN) kern = scan_tm_lean_kernel<T, MODE, HAS_Z, S>;
+    if constexpr (LEAN) kern = scan_tm_lean_kernel<T, MODE, HAS_Z, S, FLAGS>;
     else kern = scan_tm_kernel<T, MODE, HAS_Z, S, CONV, FLAGS>;
     static bool attr_set[kMaxDevices] = {};
     int dev = 0;
@@ -734,12 +738,17 @@ cudaError_t launch_tm_one(const ScanArgs &a, const TmMaps &maps, int warps, long
     return cudaGetLastError();
 }
 
-// The lean form (12..18 compute warps) of the plain direct scan, bf16 storage.
-template <int S>
+// The lean form (12..18 compute warps) of the plain direct scan, bf16 storage (FLAGS 0 or FL_CKPT).
+template <int S, int FLAGS = 0>
 cudaError_t launch_tm_lean(const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, cudaStream_t st) {
-    return a.z != nullptr ? launch_tm_one<bf16_t, MODE_FULL, true, S, false, 0, true>(a, maps, warps, Bsz, 1, st)
-                          : launch_tm_one<bf16_t, MODE_FULL, false, S, false, 0, true>(a, maps, warps, Bsz, 1, st);
+    return a.z != nullptr ? launch_tm_one<bf16_t, MODE_FULL, true, S, false, FLAGS, true>(a, maps, warps, Bsz, 1, st)
+                          : launch_tm_one<bf16_t, MODE_FULL, false, S, false, FLAGS, true>(a, maps, warps, Bsz, 1, st);
 }
+
+// The direct scan that also writes the backward pass's checkpoints (scan_tm_ckpt.cu): the regular form
+// (lean_warps == 0) or the lean form; dtype 1 = bf16, S lanes per channel.
+cudaError_t launch_tm_ckpt(int dtype, int S, const ScanArgs &a, const TmMaps &maps, int warps, bool lean,
+                           long long Bsz, cudaStream_t st);
 
 template <typename T, int S, int FLAGS = 0>
 cudaError_t launch_tm_s(int mode, const ScanArgs &a, const TmMaps &maps, int warps, long long Bsz, int gc,
