@@ -433,8 +433,9 @@ def aggregate_gbs(world, bytes_per_rank_step, t_ms, e2e_ms):
     return (world * bytes_per_rank_step / (t_ms * 1e-3) / 1e9, world * bytes_per_rank_step / (e2e_ms * 1e-3) / 1e9)
 
 
-def traffic_record(kernel_key, sources=None):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+def traffic_record(kernel_key, sources=None, kernel=None):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source
+    (and, when `kernel` is given, on that kernel instantiation)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -442,6 +443,8 @@ def traffic_record(kernel_key, sources=None):
     if not rec:
         return None
     if rec.get("source_sha") != kernel_source_sha(sources or SCAN_KERNEL_SOURCES):
+        return None
+    if kernel is not None and rec.get("kernel") != kernel:
         return None
     return rec.get("dram_bytes_per_launch")
 
@@ -602,7 +605,7 @@ def scan_result(args, m, torch, x, workload, steps, conv, t_ms, clocks, chunked,
               f"scan_tm_kernel<{io},full,z,S{S}"
               f"{',conv' if conv == 'fused' else ''}{',flags' if flag_name != 'none' else ''}>" if tm
               else f"scan_kernel<{io},NP{1 << max(2, (N - 1).bit_length())},full>")
-    traffic = traffic_record(workload)
+    traffic = traffic_record(workload, kernel=kernel)
     if t_mufu >= t_hbm:
         roof = {"bound": "alu", "achieved": round(exps / t_meas / 1e12, 4),
                 "peak": round(mufu_peak / 1e12, 4), "unit": "Tex2/s", "frac": round(t_mufu / t_meas, 4),
