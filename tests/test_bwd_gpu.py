@@ -125,6 +125,19 @@ def ckpt_geometry(N):
                                     ("f32", 16, 200), ("bf16", 4, 200), ("f32", 24, 200), ("bf16", 16, 199),
                                     ("bf16", 16, 16), ("bf16", 64, 3)])
 def test_training_pair_checkpoints_and_gradients(io, N, L):
+    """The training pair's checkpoints and gradients against the oracle (training_pair_checks)."""
+    training_pair_checks(io, N, L)
+
+
+@pytest.mark.parametrize("N", [16, 32, 64])
+def test_training_pair_lean_form(N, monkeypatch):
+    """The same checks with MAMBA_TM_LEAN=1: the lean form of the tensor-memory kernel (12..18 compute warps,
+    its checkpoint-writing instantiation) serves the forward."""
+    monkeypatch.setenv("MAMBA_TM_LEAN", "1")
+    training_pair_checks("bf16", N, 200)
+
+
+def training_pair_checks(io, N, L):
     """mamba_selective_scan_fwd_save writes y, last_state and, for every k >= 1, the state before step k * c
     (c = 16, 8, 4 for N <= 16, 32, 64): each checkpoint is compared with the oracle's last_state over the
     first k * c steps, and the padding states past N must be zero.  mamba_selective_scan_bwd_from_ckpt then
