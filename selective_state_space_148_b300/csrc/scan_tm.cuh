@@ -558,19 +558,23 @@ __device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &ma
                     } else {
                         tc::tmem_wait_ld_tied(bcu[0]);
                     }
-                    // one block: y of sub-tile i-1, Delta etc. of sub-tile i+1, the
-                    // recurrence of sub-tile i (i = 4 sup + q, so i & 1 == q & 1)
+                    // one block: y of sub-tile i-1, Delta etc. of sub-tile i+1 and the recurrence of
+                    // sub-tile i (i = 4 sup + q, so i & 1 == q & 1)
 #pragma unroll
                     for (int p = 0; p < TB / 2; ++p) dq[p] = du_chan[(q & 1) * MAX_CH * 4 + p];
                 }
-                output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
-                if (q + 1 < NSUB) {
-                    side_pair(st_cur, q + 1, r0 + (q + 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
-                } else {
-                    if (sup + 1 < nsup && !__all_sync(0xffffffffu, wait_or_abort(&io[k_nxt], ((sup + 1) / NST) & 1, false)))
-                        *abort_flag = 1;
-                    side_pair(st_nxt, 0, r0 + TT, 0, Du_r[0], g_r[0]);
-                }
+                // y of sub-tile i-1 (its Du, g), then Delta etc. of sub-tile i+1 (which reuse those registers)
+                auto side_work = [&]() {
+                    output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+                    if (q + 1 < NSUB) {
+                        side_pair(st_cur, q + 1, r0 + (q + 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+                    } else {
+                        if (sup + 1 < nsup && !__all_sync(0xffffffffu, wait_or_abort(&io[k_nxt], ((sup + 1) / NST) & 1, false)))
+                            *abort_flag = 1;
+                        side_pair(st_nxt, 0, r0 + TT, 0, Du_r[0], g_r[0]);
+                    }
+                };
+                if constexpr (!LEAN) side_work();
                 float pq[TB];
 #pragma unroll
                 for (int p = 0; p < TB / 2; ++p) {
@@ -629,6 +633,9 @@ __device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &ma
                     *reinterpret_cast<float4 *>(prow) = make_float4(pq[0], pq[1], pq[2], pq[3]);
                     *reinterpret_cast<float4 *>(prow + 4) = make_float4(pq[4], pq[5], pq[6], pq[7]);
                 }
+                // after the recurrence in the lean form: measured 2.7 % faster there on the 2.8B layer, and 8 %
+                // slower in the regular form
+                if constexpr (LEAN) side_work();
                 __syncwarp();  // partials of sub-tile i and Delta of sub-tile i+1 visible to the channel's lanes
             }
             if constexpr (CORR) {
