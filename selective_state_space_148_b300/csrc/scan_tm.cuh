@@ -578,6 +578,13 @@ __device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &ma
                 float pq[TB];
 #pragma unroll
                 for (int p = 0; p < TB / 2; ++p) {
+                    // the lean form does the side work before the sub-tile's last step pair: measured 1.1 %
+                    // faster there than after the recurrence (2.8B layer 0.4131 -> 0.4085 ms); before the
+                    // first pair (the regular form's place) it measured slower in the lean form, and the
+                    // lean form's places 1-3 % slower in the regular form
+                    if constexpr (LEAN) {
+                        if (p == TB / 2 - 1) side_work();
+                    }
                     uint32_t bcl[LEAN ? 16 : 1];
                     float4 dqp;
                     const uint32_t *bcp;
@@ -633,9 +640,6 @@ __device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &ma
                     *reinterpret_cast<float4 *>(prow) = make_float4(pq[0], pq[1], pq[2], pq[3]);
                     *reinterpret_cast<float4 *>(prow + 4) = make_float4(pq[4], pq[5], pq[6], pq[7]);
                 }
-                // after the recurrence in the lean form: measured 2.7 % faster there on the 2.8B layer, and 8 %
-                // slower in the regular form
-                if constexpr (LEAN) side_work();
                 __syncwarp();  // partials of sub-tile i and Delta of sub-tile i+1 visible to the channel's lanes
             }
             if constexpr (CORR) {
