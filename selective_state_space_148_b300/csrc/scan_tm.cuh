@@ -563,9 +563,9 @@ __device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &ma
 #pragma unroll
                     for (int p = 0; p < TB / 2; ++p) dq[p] = du_chan[(q & 1) * MAX_CH * 4 + p];
                 }
-                // y of sub-tile i-1 (its Du, g), then Delta etc. of sub-tile i+1 (which reuse those registers)
-                auto side_work = [&]() {
-                    output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+                // Delta etc. of sub-tile i+1 (into the Du, g registers of parity (i+1) & 1, which held those
+                // of sub-tile i-1)
+                auto side_only = [&]() {
                     if (q + 1 < NSUB) {
                         side_pair(st_cur, q + 1, r0 + (q + 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
                     } else {
@@ -574,7 +574,19 @@ __device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &ma
                         side_pair(st_nxt, 0, r0 + TT, 0, Du_r[0], g_r[0]);
                     }
                 };
-                if constexpr (!LEAN) side_work();
+                // y of sub-tile i-1, then the side work (the lean form's order)
+                auto side_work = [&]() {
+                    output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+                    side_only();
+                };
+                // the regular form: the side work first, then y of sub-tile i-1 from its Du, g saved before the
+                // side work reuses their registers; measured 1.4 % faster than the other order (130M layer
+                // 0.1334 -> 0.1315 ms), as was splitting the recurrence around y
+                if constexpr (!LEAN) {
+                    const float2 Du_prev = Du_r[(q + 1) & 1], g_prev = g_r[(q + 1) & 1];
+                    side_only();
+                    output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_prev, g_prev);
+                }
                 float pq[TB];
 #pragma unroll
                 for (int p = 0; p < TB / 2; ++p) {
