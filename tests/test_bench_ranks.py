@@ -61,3 +61,21 @@ def test_two_gloo_ranks_take_the_slowest_rank():
         assert t == pytest.approx(0.8) and e == pytest.approx(3.0)
         assert v == pytest.approx(2 * 1.0e9 / 0.8e-3 / 1e9)      # 2 ranks x 1 GB per step / 0.8 ms
         assert ve == pytest.approx(2 * 1.0e9 / 3.0e-3 / 1e9)
+
+
+def test_lean_form_choice_names_the_kernel_of_each_layer(monkeypatch):
+    """bench.py names the kernel a direct bf16 scan runs on (its restatement of the library's rule): the
+    regular form where it already fits in the fewest waves, the lean form at the narrowest width of fewest
+    waves otherwise, and the MAMBA_TM_LEAN override."""
+    import bench
+    monkeypatch.delenv("MAMBA_TM_LEAN", raising=False)
+    sms = 148
+    assert bench.lean_warps(8, 1536, 4, sms) == 0        # 130M layer: one wave of 11-warp CTAs already
+    assert bench.lean_warps(4, 5120, 4, sms) == 18       # 2.8B layer: one wave of 18-warp CTAs, not two
+    assert bench.lean_warps(4, 5120, 16, sms) == 18      # N = 64, 16 lanes per channel: 4 waves, not 7
+    assert bench.lean_warps(1, 21000, 4, sms) == 18      # the GPU test's widest-CTA shape
+    assert bench.lean_warps(1, 10600, 8, sms) == 18
+    monkeypatch.setenv("MAMBA_TM_LEAN", "0")
+    assert bench.lean_warps(4, 5120, 4, sms) == 0
+    monkeypatch.setenv("MAMBA_TM_LEAN", "1")
+    assert bench.lean_warps(2, 300, 4, sms) == 12        # forced: the narrowest width of fewest waves
