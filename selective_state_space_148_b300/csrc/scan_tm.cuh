@@ -574,11 +574,6 @@ __device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &ma
                         side_pair(st_nxt, 0, r0 + TT, 0, Du_r[0], g_r[0]);
                     }
                 };
-                // y of sub-tile i-1, then the side work (the lean form's order)
-                auto side_work = [&]() {
-                    output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
-                    side_only();
-                };
                 // the regular form: the side work first, then y of sub-tile i-1 from its Du, g saved before the
                 // side work reuses their registers; measured 1.4 % faster than the other order (130M layer
                 // 0.1334 -> 0.1315 ms), as was splitting the recurrence around y
@@ -590,12 +585,22 @@ __device__ __forceinline__ void scan_tm_body(const ScanArgs &a, const TmMaps &ma
                 float pq[TB];
 #pragma unroll
                 for (int p = 0; p < TB / 2; ++p) {
-                    // the lean form does the side work before the sub-tile's last step pair: measured 1.1 %
-                    // faster there than after the recurrence (2.8B layer 0.4131 -> 0.4085 ms); before the
-                    // first pair (the regular form's place) it measured slower in the lean form, and the
-                    // lean form's places 1-3 % slower in the regular form
+                    // the lean form does its side work and y of sub-tile i-1 before the sub-tile's last step
+                    // pair.  On the 2.8B layer (S = 4): 0.4246 ms before the recurrence, 0.4130 after it,
+                    // 0.4085 with y then the side work before the last pair, 0.4009 with the side work then y
+                    // (Du, g saved first); with N = 64 (S = 16) the last order measured 1.6 % slower than
+                    // y first, so S = 16 keeps y first.  These places measured 1-12 % slower in the regular form.
                     if constexpr (LEAN) {
-                        if (p == TB / 2 - 1) side_work();
+                        if (p == TB / 2 - 1) {
+                            if constexpr (S == 16) {
+                                output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_r[(q + 1) & 1], g_r[(q + 1) & 1]);
+                                side_only();
+                            } else {
+                                const float2 Du_prev = Du_r[(q + 1) & 1], g_prev = g_r[(q + 1) & 1];
+                                side_only();
+                                output_pair(r0 + (q - 1) * TB, (q + 1) & 1, Du_prev, g_prev);
+                            }
+                        }
                     }
                     uint32_t bcl[LEAN ? 16 : 1];
                     float4 dqp;
