@@ -79,3 +79,19 @@ def test_lean_form_choice_names_the_kernel_of_each_layer(monkeypatch):
     assert bench.lean_warps(4, 5120, 4, sms) == 0
     monkeypatch.setenv("MAMBA_TM_LEAN", "1")
     assert bench.lean_warps(2, 300, 4, sms) == 12        # forced: the narrowest width of fewest waves
+
+
+def test_traffic_records_apply_only_to_their_kernel_and_sources():
+    """A stored ncu DRAM traffic record is reported only for the kernel instantiation and the source hash
+    it was taken on (a flag or convolution variant of the same workload reports none)."""
+    import json
+    import bench
+    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+    r = rec["mamba130m_b8_d1536_n16_l2048_bf16"]
+    got = bench.traffic_record("mamba130m_b8_d1536_n16_l2048_bf16", kernel=r["kernel"])
+    if r["source_sha"] == bench.kernel_source_sha():
+        assert got == r["dram_bytes_per_launch"] == r["dram_read_bytes"] + r["dram_write_bytes"]
+    else:
+        assert got is None
+    assert bench.traffic_record("mamba130m_b8_d1536_n16_l2048_bf16", kernel=r["kernel"][:-1] + ",flags>") is None
+    assert bench.traffic_record("no_such_workload") is None
